@@ -1,0 +1,229 @@
+/*
+ * ct.h -- C ABI of the GB300 forward transposed-convolution library (libct.so).
+ *
+ * The operation.  y = ConvTranspose(x, w, bias): the transpose of a
+ * convolution ("fractionally strided convolution", "deconvolution"), as
+ * described on the ONNX page "ai.onnx.ConvTranspose" (Description) with the
+ * PyTorch conventions stated in "feat(ops): implement convTranspose2d -- CPU
+ * kernel, backward and StableHLO lowering" (SKaiNET #1464, Summary):
+ *
+ *   y[b, oc, o] = bias[oc]
+ *               + sum over ic in oc's group, taps t, inputs i with
+ *                 o_a = i_a*stride_a - pad_lo_a + t_a*dilation_a on every axis a
+ *                 of x[b, ic, i] * w[ic, oc mod (C_out/groups), t]
+ *
+ * i.e. each input sample is scattered through every weight tap, and products
+ * that land outside the output are dropped.  Per spatial axis the output
+ * extent is
+ *
+ *   O_a = (I_a - 1)*stride_a - pad_lo_a - pad_hi_a + dilation_a*(k_a - 1)
+ *         + output_padding_a + 1
+ *
+ * (SKaiNET #1464, Summary, output size; asymmetric per-side padding as in the
+ * NKI page "Conv3D Transpose Kernel API Reference", conv3d_transpose
+ * parameters).  output_padding extends the high end of each axis.
+ *
+ * Layouts (all dense, row-major, one dtype for x, w, bias and y):
+ *   x    [B, C_in, I_1 .. I_nd]                 (NCL / NCHW / NCDHW)
+ *   w    [C_in, C_out/groups, k_1 .. k_nd]       (PyTorch ConvTranspose layout)
+ *   bias [C_out] or NULL
+ *   y    [B, C_out, O_1 .. O_nd]
+ * Accumulation is in fp32 for every dtype; bias is added in fp32 and the sum
+ * is rounded once (round-to-nearest-even) to the output dtype.
+ *
+ * Conventions for every entry point:
+ *   - Return value is a ct_status; CT_OK (0) on success.  On any other value
+ *     ct_last_error() gives a message (thread-local, valid until the next
+ *     failing call from the same thread).
+ *   - Argument validation happens on the host before any device work; a
+ *     rejected call launches nothing and leaves y untouched.
+ *   - Arrays of per-axis values (in_spatial, k, stride, pad_lo, pad_hi,
+ *     dilation, output_padding) hold nd entries each, outermost axis first.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Device entry points are asynchronous on that stream.
+ *   - The library holds no per-call state; calls on different streams may run
+ *     concurrently provided they use distinct workspaces.
+ */
+#ifndef CT_H
+#define CT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types.  Integer types are not accepted ("dtype guard so non-float
+ * dtypes fail loudly", SKaiNET #1464, Summary). */
+typedef enum { CT_F32 = 0, CT_F16 = 1, CT_BF16 = 2 } ct_dtype;
+
+typedef enum {
+    CT_OK = 0,
+    CT_ERR_NULL = 1,            /* a required pointer is NULL */
+    CT_ERR_RANK = 2,            /* nd outside 1..3 */
+    CT_ERR_SHAPE = 3,           /* negative size, or an output extent < 1 */
+    CT_ERR_PARAM = 4,           /* k, stride, dilation < 1; pad < 0;
+                                   output_padding outside [0, max(stride, dilation)) */
+    CT_ERR_GROUPS = 5,          /* groups < 1 or not dividing C_in and C_out */
+    CT_ERR_BIAS = 6,            /* bias shape is not [C_out] (binding-level check) */
+    CT_ERR_DTYPE = 7,           /* dtype is not one of ct_dtype */
+    CT_ERR_CUDA = 8,            /* a CUDA runtime call or launch failed */
+    CT_ERR_DEVICE_TIMEOUT = 9,  /* a bounded device-side wait gave up */
+    CT_ERR_WORKSPACE = 10,      /* workspace given but smaller than required */
+    CT_ERR_ALIGN = 11,          /* a pointer is not aligned to its element size */
+    CT_ERR_ROUTE = 12,          /* a forced route cannot run this problem */
+    CT_ERR_TOO_LARGE = 13       /* a size exceeds what the kernels index */
+} ct_status;
+
+/* Kernel routes.  CT_ROUTE_AUTO lets the library choose per call from the
+ * shapes and dtype, as the ONNX page's "Implementation variants" section
+ * describes one variant being selected per call. */
+typedef enum {
+    CT_ROUTE_AUTO = -1,
+    CT_ROUTE_NONE = 0,      /* y has no elements: nothing to do */
+    CT_ROUTE_BIAS_FILL = 1, /* no input contributes (C_in == 0 or an input
+                               extent is 0): y = bias broadcast, or 0 */
+    CT_ROUTE_GATHER = 2,    /* generic CUDA-core gather, any shape and dtype */
+    CT_ROUTE_GROUPED = 3,   /* CUDA-core grouped/depthwise stride-phase gather */
+    CT_ROUTE_SIMT_GEMM = 4, /* fp32 stride-phase implicit GEMM on CUDA cores */
+    CT_ROUTE_TC_GEMM = 5    /* bf16/fp16 stride-phase implicit GEMM on tcgen05 */
+} ct_route;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int ct_version(void);
+
+/* Message for the last nonzero status returned on this thread. */
+const char* ct_last_error(void);
+
+/* Fixed text for a status code. */
+const char* ct_status_string(int status);
+
+/*
+ * Output spatial extents (host only, no device work).  The shape-only
+ * counterpart of the operation (SKaiNET #1464: "VoidTensorOps: shape-only
+ * implementation"; ONNX page: output shapes are inferred from the inputs and
+ * attributes).  Writes nd values to out_spatial.
+ * Errors: CT_ERR_NULL, CT_ERR_RANK, CT_ERR_SHAPE, CT_ERR_PARAM, CT_ERR_TOO_LARGE.
+ */
+int ct_conv_transpose_out_shape(int nd, const int64_t* in_spatial,
+                                const int64_t* k, const int* stride,
+                                const int* pad_lo, const int* pad_hi,
+                                const int* dilation, const int* output_padding,
+                                int64_t* out_spatial);
+
+/*
+ * Bytes of device workspace ct_conv_transpose_nd needs for this problem on
+ * the route it would choose (0 when the route needs none).  The workspace
+ * holds the reordered (tap-reversed, per-phase, K-major) weights and, for the
+ * tensor-core route, a channels-last copy of x.  Host only.
+ * Errors: the validation errors of ct_conv_transpose_nd.
+ */
+int ct_conv_transpose_workspace_bytes(int nd, int64_t B, int64_t C_in,
+                                      int64_t C_out, const int64_t* in_spatial,
+                                      const int64_t* k, const int* stride,
+                                      const int* pad_lo, const int* pad_hi,
+                                      const int* dilation,
+                                      const int* output_padding, int groups,
+                                      int dtype, size_t* bytes);
+
+/*
+ * The route ct_conv_transpose_nd would take for this problem (a ct_route
+ * value written to *route).  Host only; the route also depends on the current
+ * device (the tensor-core route needs an sm_103 device).
+ */
+int ct_conv_transpose_route(int nd, int64_t B, int64_t C_in, int64_t C_out,
+                            const int64_t* in_spatial, const int64_t* k,
+                            const int* stride, const int* pad_lo,
+                            const int* pad_hi, const int* dilation,
+                            const int* output_padding, int groups, int dtype,
+                            int* route);
+
+/*
+ * Forward transposed convolution on the device.
+ *
+ *   x, w, bias, y : device pointers owned by the caller, layouts above; bias
+ *                   may be NULL.  x, w and bias are only read; y is fully
+ *                   overwritten (every element, including positions no input
+ *                   reaches, which receive bias or 0).  y must not overlap
+ *                   x, w, bias or the workspace.
+ *   workspace     : device memory of at least ct_conv_transpose_workspace_bytes
+ *                   bytes, 256-byte aligned, or NULL.  When NULL and the route
+ *                   needs workspace, the call takes it from the stream-ordered
+ *                   allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
+ *   workspace_bytes : size of `workspace` (ignored when workspace is NULL).
+ *   nd            : number of spatial axes, 1..3.
+ *   B, C_in, C_out, groups : batch, channels and groups; C_out = w.shape[1]*groups.
+ *   dtype         : ct_dtype of x, w, bias and y.
+ *   stream        : cudaStream_t (as void*).
+ *
+ * Pointers must be aligned to the element size (CT_ERR_ALIGN otherwise); the
+ * fast routes additionally want 16-byte alignment and otherwise fall back to
+ * the generic gather route.  Launch failures return CT_ERR_CUDA.  The call
+ * does not synchronise.
+ */
+int ct_conv_transpose_nd(const void* x, const void* w, const void* bias,
+                         void* y, void* workspace, size_t workspace_bytes,
+                         int nd, int64_t B, int64_t C_in, int64_t C_out,
+                         const int64_t* in_spatial, const int64_t* k,
+                         const int* stride, const int* pad_lo,
+                         const int* pad_hi, const int* dilation,
+                         const int* output_padding, int groups, int dtype,
+                         void* stream);
+
+/*
+ * As ct_conv_transpose_nd, with the kernel route chosen by the caller
+ * (CT_ROUTE_AUTO = the library's choice).  A route that cannot run the
+ * problem returns CT_ERR_ROUTE.  Used to test every route on the same inputs.
+ * The workspace, when given, must be sized for the forced route
+ * (ct_conv_transpose_route_workspace_bytes).
+ */
+int ct_conv_transpose_nd_route(const void* x, const void* w, const void* bias,
+                               void* y, void* workspace, size_t workspace_bytes,
+                               int nd, int64_t B, int64_t C_in, int64_t C_out,
+                               const int64_t* in_spatial, const int64_t* k,
+                               const int* stride, const int* pad_lo,
+                               const int* pad_hi, const int* dilation,
+                               const int* output_padding, int groups,
+                               int dtype, int route, void* stream);
+
+/* Workspace bytes of a given route (CT_ERR_ROUTE if it cannot run the problem). */
+int ct_conv_transpose_route_workspace_bytes(int nd, int64_t B, int64_t C_in,
+                                            int64_t C_out,
+                                            const int64_t* in_spatial,
+                                            const int64_t* k, const int* stride,
+                                            const int* pad_lo, const int* pad_hi,
+                                            const int* dilation,
+                                            const int* output_padding,
+                                            int groups, int dtype, int route,
+                                            size_t* bytes);
+
+/*
+ * End-to-end call on HOST buffers: x, w, bias (nullable) and y are host
+ * pointers (pinned memory gives the fastest copies).  The call allocates
+ * device buffers stream-ordered, copies the inputs to the device, runs
+ * ct_conv_transpose_nd, copies y back, frees the buffers and synchronises
+ * `stream` before returning.  Same validation and errors as the device call.
+ */
+int ct_conv_transpose_nd_host(const void* x, const void* w, const void* bias,
+                              void* y, int nd, int64_t B, int64_t C_in,
+                              int64_t C_out, const int64_t* in_spatial,
+                              const int64_t* k, const int* stride,
+                              const int* pad_lo, const int* pad_hi,
+                              const int* dilation, const int* output_padding,
+                              int groups, int dtype, void* stream);
+
+/*
+ * Device-side error word written by bounded waits in the tensor-core kernel
+ * (0 = none; otherwise the code says which wait gave up).  Synchronises the
+ * current device, writes the word to *code and clears it when `clear` is
+ * nonzero.  Returns CT_ERR_DEVICE_TIMEOUT when the word was set, CT_OK
+ * otherwise.
+ */
+int ct_device_status(int clear, unsigned int* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CT_H */

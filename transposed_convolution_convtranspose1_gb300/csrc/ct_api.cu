@@ -1,0 +1,399 @@
+// ct_api.cu -- host side of the C ABI: validation, output shape, stride-phase
+// plan, route choice, workspace sizing and dispatch.  No device code here.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "ct_internal.h"
+#include "ct_routes.h"
+
+namespace ct {
+namespace {
+
+thread_local char g_msg[512] = "";
+
+int fail(int status, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+    return fail(CT_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Output extent of one axis (SKaiNET #1464 Summary "output size", with the
+// NKI page's separate low/high pads).
+int64_t out_extent(int64_t I, int64_t K, int64_t S, int64_t PL, int64_t PH, int64_t DL,
+                   int64_t OP) {
+    return (I - 1) * S - PL - PH + DL * (K - 1) + OP + 1;
+}
+
+// Checks the per-axis attributes and fills the normalised axis fields.
+// The rules are those SKaiNET #1464 lists for its CPU kernel: positive
+// stride and dilation, non-negative padding and
+// output_padding < max(stride, dilation) per axis.
+int fill_axes(Problem* p, int nd, const int64_t* in_spatial, const int64_t* k, const int* stride,
+              const int* pad_lo, const int* pad_hi, const int* dilation,
+              const int* output_padding) {
+    if (nd < 1 || nd > 3) return fail(CT_ERR_RANK, "nd must be 1, 2 or 3 (got %d)", nd);
+    if (!in_spatial || !k || !stride || !pad_lo || !pad_hi || !dilation || !output_padding)
+        return fail(CT_ERR_NULL, "a per-axis attribute array is NULL");
+    p->nd = nd;
+    for (int a = 0; a < 3; ++a) {
+        p->I[a] = 1; p->K[a] = 1; p->O[a] = 1;
+        p->S[a] = 1; p->PL[a] = 0; p->PH[a] = 0; p->DL[a] = 1; p->OP[a] = 0;
+    }
+    for (int j = 0; j < nd; ++j) {
+        const int a = 3 - nd + j;
+        if (in_spatial[j] < 0) return fail(CT_ERR_SHAPE, "input extent of axis %d is negative", j);
+        if (k[j] < 1) return fail(CT_ERR_PARAM, "kernel size of axis %d must be >= 1", j);
+        if (stride[j] < 1) return fail(CT_ERR_PARAM, "stride of axis %d must be >= 1", j);
+        if (dilation[j] < 1) return fail(CT_ERR_PARAM, "dilation of axis %d must be >= 1", j);
+        if (pad_lo[j] < 0 || pad_hi[j] < 0)
+            return fail(CT_ERR_PARAM, "padding of axis %d must be >= 0", j);
+        const int lim = stride[j] > dilation[j] ? stride[j] : dilation[j];
+        if (output_padding[j] < 0 || output_padding[j] >= lim)
+            return fail(CT_ERR_PARAM,
+                        "output_padding of axis %d must be in [0, max(stride, dilation)) = [0, %d)",
+                        j, lim);
+        if (k[j] > kMaxK || stride[j] > kMaxStride)
+            return fail(CT_ERR_TOO_LARGE, "axis %d: kernel size <= %d and stride <= %d supported", j,
+                        kMaxK, kMaxStride);
+        if (in_spatial[j] > (1ll << 30) || dilation[j] > (1 << 20) || pad_lo[j] > (1 << 30) ||
+            pad_hi[j] > (1 << 30))
+            return fail(CT_ERR_TOO_LARGE, "axis %d: size or attribute too large", j);
+        p->I[a] = in_spatial[j]; p->K[a] = k[j]; p->S[a] = stride[j];
+        p->PL[a] = pad_lo[j]; p->PH[a] = pad_hi[j]; p->DL[a] = dilation[j];
+        p->OP[a] = output_padding[j];
+        p->O[a] = out_extent(p->I[a], p->K[a], p->S[a], p->PL[a], p->PH[a], p->DL[a], p->OP[a]);
+        if (p->O[a] < 1)
+            return fail(CT_ERR_SHAPE, "output extent of axis %d would be %lld (< 1)", j,
+                        (long long)p->O[a]);
+        if (p->O[a] > (1ll << 31) - 1)
+            return fail(CT_ERR_TOO_LARGE, "output extent of axis %d exceeds 2^31-1", j);
+    }
+    return CT_OK;
+}
+
+int validate(Problem* p, int nd, int64_t B, int64_t C_in, int64_t C_out, const int64_t* in_spatial,
+             const int64_t* k, const int* stride, const int* pad_lo, const int* pad_hi,
+             const int* dilation, const int* output_padding, int groups, int dtype) {
+    std::memset(p, 0, sizeof(*p));
+    int rc = fill_axes(p, nd, in_spatial, k, stride, pad_lo, pad_hi, dilation, output_padding);
+    if (rc != CT_OK) return rc;
+    if (dtype != CT_F32 && dtype != CT_F16 && dtype != CT_BF16)
+        return fail(CT_ERR_DTYPE,
+                    "dtype %d is not a supported floating type (CT_F32, CT_F16, CT_BF16)", dtype);
+    if (B < 0 || C_in < 0 || C_out < 0) return fail(CT_ERR_SHAPE, "B, C_in and C_out must be >= 0");
+    if (groups < 1) return fail(CT_ERR_GROUPS, "groups must be >= 1 (got %d)", groups);
+    if (C_in % groups != 0 || C_out % groups != 0)
+        return fail(CT_ERR_GROUPS, "groups=%d must divide C_in=%lld and C_out=%lld", groups,
+                    (long long)C_in, (long long)C_out);
+    if (C_in > (1 << 24) || C_out > (1 << 24) || B > (1ll << 31))
+        return fail(CT_ERR_TOO_LARGE, "B, C_in or C_out too large");
+    p->B = B; p->C_in = C_in; p->C_out = C_out; p->G = groups;
+    p->Cig = (int)(C_in / groups); p->Cog = (int)(C_out / groups);
+    p->dtype = (ct_dtype)dtype;
+    const double xe = (double)B * C_in * p->in_spatial();
+    const double ye = (double)B * C_out * p->out_spatial();
+    const double we = (double)C_in * p->Cog * p->taps();
+    if (xe > 4e18 || ye > 4e18 || we > 4e18) return fail(CT_ERR_TOO_LARGE, "tensor too large");
+    return CT_OK;
+}
+
+bool aligned(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
+
+bool route_supports(const Problem& p, int route) {
+    const bool empty_out = p.y_elems() == 0;
+    const bool no_input = p.C_in == 0 || p.in_spatial() == 0;
+    switch (route) {
+        case CT_ROUTE_NONE: return empty_out;
+        case CT_ROUTE_BIAS_FILL: return !empty_out && no_input;
+        case CT_ROUTE_GATHER: return !empty_out && !no_input;
+        case CT_ROUTE_GROUPED: return !empty_out && !no_input && grouped_supports(p);
+        case CT_ROUTE_SIMT_GEMM: return !empty_out && !no_input && simt_supports(p);
+        case CT_ROUTE_TC_GEMM: return !empty_out && !no_input && tc_supports(p);
+        default: return false;
+    }
+}
+
+int choose_route(const Problem& p) {
+    if (p.y_elems() == 0) return CT_ROUTE_NONE;
+    if (p.C_in == 0 || p.in_spatial() == 0) return CT_ROUTE_BIAS_FILL;
+    if (route_supports(p, CT_ROUTE_TC_GEMM) && tc_preferred(p)) return CT_ROUTE_TC_GEMM;
+    if (route_supports(p, CT_ROUTE_SIMT_GEMM) && simt_preferred(p)) return CT_ROUTE_SIMT_GEMM;
+    if (route_supports(p, CT_ROUTE_GROUPED) && grouped_preferred(p)) return CT_ROUTE_GROUPED;
+    return CT_ROUTE_GATHER;
+}
+
+size_t route_workspace(const Problem& p, int route) {
+    switch (route) {
+        case CT_ROUTE_SIMT_GEMM: return simt_workspace_bytes(p);
+        case CT_ROUTE_TC_GEMM: return tc_workspace_bytes(p);
+        default: return 0;
+    }
+}
+
+int run(const Problem& p, int route, const void* x, const void* w, const void* bias, void* y,
+        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    const size_t need = route_workspace(p, route);
+    void* ws = workspace;
+    bool owned = false;
+    if (need > 0) {
+        if (ws) {
+            if (workspace_bytes < need)
+                return fail(CT_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
+                            workspace_bytes, need);
+            if (!aligned(ws, 256)) return fail(CT_ERR_ALIGN, "workspace must be 256-byte aligned");
+        } else {
+            cudaError_t e = cudaMallocAsync(&ws, need, stream);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(workspace)");
+            owned = true;
+        }
+    }
+    cudaError_t e = cudaSuccess;
+    switch (route) {
+        case CT_ROUTE_NONE: break;
+        case CT_ROUTE_BIAS_FILL: e = launch_bias_fill(p, bias, y, stream); break;
+        case CT_ROUTE_GATHER: e = launch_gather(p, x, w, bias, y, stream); break;
+        case CT_ROUTE_GROUPED: e = launch_grouped(p, x, w, bias, y, stream); break;
+        case CT_ROUTE_SIMT_GEMM: e = launch_simt(p, x, w, bias, y, ws, stream); break;
+        case CT_ROUTE_TC_GEMM: e = launch_tc(p, x, w, bias, y, ws, stream); break;
+        default: e = cudaErrorInvalidValue; break;
+    }
+    if (owned) {
+        cudaError_t e2 = cudaFreeAsync(ws, stream);
+        if (e == cudaSuccess) e = e2;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return CT_OK;
+}
+
+int check_pointers(const Problem& p, const void* x, const void* w, const void* bias, const void* y) {
+    if (p.x_elems() > 0 && !x) return fail(CT_ERR_NULL, "x is NULL");
+    if (p.w_elems() > 0 && !w) return fail(CT_ERR_NULL, "w is NULL");
+    if (p.y_elems() > 0 && !y) return fail(CT_ERR_NULL, "y is NULL");
+    const size_t eb = p.elem_bytes();
+    if (!aligned(x, eb) || !aligned(w, eb) || !aligned(y, eb) || !aligned(bias, eb))
+        return fail(CT_ERR_ALIGN, "pointers must be aligned to the element size (%zu bytes)", eb);
+    return CT_OK;
+}
+
+}  // namespace
+
+void plan_axis(const Problem& p, int axis, AxisPlan* out) {
+    const int s = p.S[axis];
+    out->s = s;
+    for (int r = 0; r < s; ++r) {
+        out->q_extent[r] = (r < p.O[axis]) ? (p.O[axis] - r + s - 1) / s : 0;
+        int n = 0;
+        // Walk taps from high to low so that input offsets come out increasing.
+        for (int t = (int)p.K[axis] - 1; t >= 0; --t) {
+            const int64_t v = (int64_t)r + p.PL[axis] - (int64_t)t * p.DL[axis];
+            const int64_t m = ((v % s) + s) % s;
+            if (m != 0) continue;
+            out->tap[r][n] = t;
+            out->off[r][n] = (int)(v / s);  // exact: v is a multiple of s
+            ++n;
+        }
+        out->ntaps[r] = n;
+    }
+}
+
+cudaError_t device_info(DeviceInfo* out) {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    static bool have[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && have[dev]) {
+        *out = cache[dev];
+        return cudaSuccess;
+    }
+    DeviceInfo d{};
+    d.device = dev;
+    if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return e;
+    int optin = 0;
+    if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+    d.smem_optin = (size_t)optin;
+    if (dev >= 0 && dev < 64) {
+        cache[dev] = d;
+        have[dev] = true;
+    }
+    *out = d;
+    return cudaSuccess;
+}
+
+}  // namespace ct
+
+using namespace ct;
+
+extern "C" {
+
+int ct_version(void) { return 100; }
+
+const char* ct_last_error(void) { return g_msg; }
+
+const char* ct_status_string(int status) {
+    switch (status) {
+        case CT_OK: return "CT_OK";
+        case CT_ERR_NULL: return "CT_ERR_NULL";
+        case CT_ERR_RANK: return "CT_ERR_RANK";
+        case CT_ERR_SHAPE: return "CT_ERR_SHAPE";
+        case CT_ERR_PARAM: return "CT_ERR_PARAM";
+        case CT_ERR_GROUPS: return "CT_ERR_GROUPS";
+        case CT_ERR_BIAS: return "CT_ERR_BIAS";
+        case CT_ERR_DTYPE: return "CT_ERR_DTYPE";
+        case CT_ERR_CUDA: return "CT_ERR_CUDA";
+        case CT_ERR_DEVICE_TIMEOUT: return "CT_ERR_DEVICE_TIMEOUT";
+        case CT_ERR_WORKSPACE: return "CT_ERR_WORKSPACE";
+        case CT_ERR_ALIGN: return "CT_ERR_ALIGN";
+        case CT_ERR_ROUTE: return "CT_ERR_ROUTE";
+        case CT_ERR_TOO_LARGE: return "CT_ERR_TOO_LARGE";
+        default: return "unknown status";
+    }
+}
+
+int ct_conv_transpose_out_shape(int nd, const int64_t* in_spatial, const int64_t* k,
+                                const int* stride, const int* pad_lo, const int* pad_hi,
+                                const int* dilation, const int* output_padding,
+                                int64_t* out_spatial) {
+    Problem p;
+    std::memset(&p, 0, sizeof(p));
+    int rc = fill_axes(&p, nd, in_spatial, k, stride, pad_lo, pad_hi, dilation, output_padding);
+    if (rc != CT_OK) return rc;
+    if (!out_spatial) return fail(CT_ERR_NULL, "out_spatial is NULL");
+    for (int j = 0; j < nd; ++j) out_spatial[j] = p.O[3 - nd + j];
+    return CT_OK;
+}
+
+int ct_conv_transpose_route(int nd, int64_t B, int64_t C_in, int64_t C_out,
+                            const int64_t* in_spatial, const int64_t* k, const int* stride,
+                            const int* pad_lo, const int* pad_hi, const int* dilation,
+                            const int* output_padding, int groups, int dtype, int* route) {
+    Problem p;
+    int rc = validate(&p, nd, B, C_in, C_out, in_spatial, k, stride, pad_lo, pad_hi, dilation,
+                      output_padding, groups, dtype);
+    if (rc != CT_OK) return rc;
+    if (!route) return fail(CT_ERR_NULL, "route is NULL");
+    *route = choose_route(p);
+    return CT_OK;
+}
+
+int ct_conv_transpose_route_workspace_bytes(int nd, int64_t B, int64_t C_in, int64_t C_out,
+                                            const int64_t* in_spatial, const int64_t* k,
+                                            const int* stride, const int* pad_lo,
+                                            const int* pad_hi, const int* dilation,
+                                            const int* output_padding, int groups, int dtype,
+                                            int route, size_t* bytes) {
+    Problem p;
+    int rc = validate(&p, nd, B, C_in, C_out, in_spatial, k, stride, pad_lo, pad_hi, dilation,
+                      output_padding, groups, dtype);
+    if (rc != CT_OK) return rc;
+    if (!bytes) return fail(CT_ERR_NULL, "bytes is NULL");
+    if (route == CT_ROUTE_AUTO) route = choose_route(p);
+    if (!route_supports(p, route)) return fail(CT_ERR_ROUTE, "route %d cannot run this problem", route);
+    *bytes = route_workspace(p, route);
+    return CT_OK;
+}
+
+int ct_conv_transpose_workspace_bytes(int nd, int64_t B, int64_t C_in, int64_t C_out,
+                                      const int64_t* in_spatial, const int64_t* k,
+                                      const int* stride, const int* pad_lo, const int* pad_hi,
+                                      const int* dilation, const int* output_padding, int groups,
+                                      int dtype, size_t* bytes) {
+    return ct_conv_transpose_route_workspace_bytes(nd, B, C_in, C_out, in_spatial, k, stride,
+                                                   pad_lo, pad_hi, dilation, output_padding,
+                                                   groups, dtype, CT_ROUTE_AUTO, bytes);
+}
+
+int ct_conv_transpose_nd_route(const void* x, const void* w, const void* bias, void* y,
+                               void* workspace, size_t workspace_bytes, int nd, int64_t B,
+                               int64_t C_in, int64_t C_out, const int64_t* in_spatial,
+                               const int64_t* k, const int* stride, const int* pad_lo,
+                               const int* pad_hi, const int* dilation, const int* output_padding,
+                               int groups, int dtype, int route, void* stream) {
+    Problem p;
+    int rc = validate(&p, nd, B, C_in, C_out, in_spatial, k, stride, pad_lo, pad_hi, dilation,
+                      output_padding, groups, dtype);
+    if (rc != CT_OK) return rc;
+    rc = check_pointers(p, x, w, bias, y);
+    if (rc != CT_OK) return rc;
+    if (route == CT_ROUTE_AUTO) {
+        route = choose_route(p);
+    } else if (!route_supports(p, route)) {
+        return fail(CT_ERR_ROUTE, "route %d cannot run this problem", route);
+    }
+    return run(p, route, x, w, bias, y, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+int ct_conv_transpose_nd(const void* x, const void* w, const void* bias, void* y, void* workspace,
+                         size_t workspace_bytes, int nd, int64_t B, int64_t C_in, int64_t C_out,
+                         const int64_t* in_spatial, const int64_t* k, const int* stride,
+                         const int* pad_lo, const int* pad_hi, const int* dilation,
+                         const int* output_padding, int groups, int dtype, void* stream) {
+    return ct_conv_transpose_nd_route(x, w, bias, y, workspace, workspace_bytes, nd, B, C_in, C_out,
+                                      in_spatial, k, stride, pad_lo, pad_hi, dilation,
+                                      output_padding, groups, dtype, CT_ROUTE_AUTO, stream);
+}
+
+int ct_conv_transpose_nd_host(const void* x, const void* w, const void* bias, void* y, int nd,
+                              int64_t B, int64_t C_in, int64_t C_out, const int64_t* in_spatial,
+                              const int64_t* k, const int* stride, const int* pad_lo,
+                              const int* pad_hi, const int* dilation, const int* output_padding,
+                              int groups, int dtype, void* stream) {
+    Problem p;
+    int rc = validate(&p, nd, B, C_in, C_out, in_spatial, k, stride, pad_lo, pad_hi, dilation,
+                      output_padding, groups, dtype);
+    if (rc != CT_OK) return rc;
+    rc = check_pointers(p, x, w, bias, y);
+    if (rc != CT_OK) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t eb = p.elem_bytes();
+    const size_t xb = (size_t)p.x_elems() * eb, wb = (size_t)p.w_elems() * eb;
+    const size_t bb = bias ? (size_t)p.C_out * eb : 0, yb = (size_t)p.y_elems() * eb;
+    auto round = [](size_t n) { return (n + 255) / 256 * 256; };
+    const size_t ws = route_workspace(p, choose_route(p));
+    const size_t total = round(xb) + round(wb) + round(bb) + round(yb) + round(ws);
+    char* base = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (total > 0) {
+        e = cudaMallocAsync((void**)&base, total, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(host call buffers)");
+    }
+    char* dx = base;
+    char* dw = dx + round(xb);
+    char* db = dw + round(wb);
+    char* dy = db + round(bb);
+    char* dws = dy + round(yb);
+    if (xb) e = cudaMemcpyAsync(dx, x, xb, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && wb) e = cudaMemcpyAsync(dw, w, wb, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && bb) e = cudaMemcpyAsync(db, bias, bb, cudaMemcpyHostToDevice, s);
+    rc = CT_OK;
+    if (e != cudaSuccess) {
+        rc = cuda_fail(e, "cudaMemcpyAsync(host to device)");
+    } else {
+        rc = ct_conv_transpose_nd(dx, dw, bias ? db : nullptr, dy, ws ? dws : nullptr, ws, nd, B,
+                                  C_in, C_out, in_spatial, k, stride, pad_lo, pad_hi, dilation,
+                                  output_padding, groups, dtype, stream);
+        if (rc == CT_OK && yb) {
+            e = cudaMemcpyAsync(y, dy, yb, cudaMemcpyDeviceToHost, s);
+            if (e != cudaSuccess) rc = cuda_fail(e, "cudaMemcpyAsync(device to host)");
+        }
+    }
+    if (base) cudaFreeAsync(base, s);
+    e = cudaStreamSynchronize(s);
+    if (rc == CT_OK && e != cudaSuccess) rc = cuda_fail(e, "cudaStreamSynchronize");
+    return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// ct_internal.h -- shared declarations of the CUDA library behind include/ct.h.
+//
+// Every problem is normalised to three spatial axes (0 = D, 1 = H, 2 = W);
+// the unused leading axes of a 1-D or 2-D problem have extent 1, kernel 1,
+// stride 1, no padding and dilation 1, which leaves the result unchanged.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "ct.h"
+
+namespace ct {
+
+// Per-axis limits the planner and kernels rely on.
+constexpr int kMaxK = 32;        // kernel taps per axis
+constexpr int kMaxStride = 32;   // stride per axis
+constexpr int kMaxPhaseTaps = 32;
+
+struct Problem {
+    int nd;
+    int64_t B, C_in, C_out;
+    int G, Cig, Cog;
+    int64_t I[3], K[3], O[3];
+    int S[3], PL[3], PH[3], DL[3], OP[3];
+    ct_dtype dtype;
+
+    int64_t in_spatial() const { return I[0] * I[1] * I[2]; }
+    int64_t out_spatial() const { return O[0] * O[1] * O[2]; }
+    int64_t taps() const { return K[0] * K[1] * K[2]; }
+    int64_t x_elems() const { return B * C_in * in_spatial(); }
+    int64_t y_elems() const { return B * C_out * out_spatial(); }
+    int64_t w_elems() const { return C_in * (int64_t)Cog * taps(); }
+    size_t elem_bytes() const { return dtype == CT_F32 ? 4 : 2; }
+};
+
+// Stride-phase plan of one axis.  Output o = r + s*q (residue r in [0, s))
+// receives tap t exactly when (r + pad_lo - t*d) is a multiple of s; that tap
+// then reads input i = q + off with off = (r + pad_lo - t*d) / s.  Taps are
+// listed in increasing input offset, i.e. in reversed tap order.
+struct AxisPlan {
+    int s;                              // number of residues (= stride)
+    int64_t q_extent[kMaxStride];       // #q with r + s*q < O, per residue
+    int ntaps[kMaxStride];
+    int tap[kMaxStride][kMaxPhaseTaps];
+    int off[kMaxStride][kMaxPhaseTaps];
+};
+
+void plan_axis(const Problem& p, int axis, AxisPlan* out);
+
+// Device properties cached per device.
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int cc_major, cc_minor;
+    size_t smem_optin;
+};
+cudaError_t device_info(DeviceInfo* out);
+
+// Launchers.  Each returns the first CUDA error it met (cudaSuccess if none).
+cudaError_t launch_bias_fill(const Problem& p, const void* bias, void* y,
+                             cudaStream_t stream);
+cudaError_t launch_gather(const Problem& p, const void* x, const void* w,
+                          const void* bias, void* y, cudaStream_t stream);
+
+}  // namespace ct
