@@ -187,6 +187,26 @@ int ct_conv_transpose_nd_route(const void* x, const void* w, const void* bias,
                                const int* output_padding, int groups,
                                int dtype, int route, void* stream);
 
+/*
+ * As ct_conv_transpose_nd_route, for measurement.  main_start / main_stop
+ * (cudaEvent_t as void*, either may be NULL) are recorded on `stream` just
+ * before and just after the launch of the route's dominant kernel, so the
+ * caller can time that kernel alone with cudaEventElapsedTime.  *launches
+ * (nullable) receives the number of kernels the call launched and
+ * *route_taken (nullable) the route that ran.
+ */
+int ct_conv_transpose_nd_profiled(const void* x, const void* w, const void* bias,
+                                  void* y, void* workspace,
+                                  size_t workspace_bytes, int nd, int64_t B,
+                                  int64_t C_in, int64_t C_out,
+                                  const int64_t* in_spatial, const int64_t* k,
+                                  const int* stride, const int* pad_lo,
+                                  const int* pad_hi, const int* dilation,
+                                  const int* output_padding, int groups,
+                                  int dtype, int route, void* stream,
+                                  void* main_start, void* main_stop,
+                                  int* launches, int* route_taken);
+
 /* Workspace bytes of a given route (CT_ERR_ROUTE if it cannot run the problem). */
 int ct_conv_transpose_route_workspace_bytes(int nd, int64_t B, int64_t C_in,
                                             int64_t C_out,

@@ -140,7 +140,7 @@ size_t route_workspace(const Problem& p, int route) {
 }
 
 int run(const Problem& p, int route, const void* x, const void* w, const void* bias, void* y,
-        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+        void* workspace, size_t workspace_bytes, cudaStream_t stream, Profile* prof) {
     const size_t need = route_workspace(p, route);
     void* ws = workspace;
     bool owned = false;
@@ -159,11 +159,11 @@ int run(const Problem& p, int route, const void* x, const void* w, const void* b
     cudaError_t e = cudaSuccess;
     switch (route) {
         case CT_ROUTE_NONE: break;
-        case CT_ROUTE_BIAS_FILL: e = launch_bias_fill(p, bias, y, stream); break;
-        case CT_ROUTE_GATHER: e = launch_gather(p, x, w, bias, y, stream); break;
-        case CT_ROUTE_GROUPED: e = launch_grouped(p, x, w, bias, y, stream); break;
-        case CT_ROUTE_SIMT_GEMM: e = launch_simt(p, x, w, bias, y, ws, stream); break;
-        case CT_ROUTE_TC_GEMM: e = launch_tc(p, x, w, bias, y, ws, stream); break;
+        case CT_ROUTE_BIAS_FILL: e = launch_bias_fill(p, bias, y, stream, prof); break;
+        case CT_ROUTE_GATHER: e = launch_gather(p, x, w, bias, y, stream, prof); break;
+        case CT_ROUTE_GROUPED: e = launch_grouped(p, x, w, bias, y, stream, prof); break;
+        case CT_ROUTE_SIMT_GEMM: e = launch_simt(p, x, w, bias, y, ws, stream, prof); break;
+        case CT_ROUTE_TC_GEMM: e = launch_tc(p, x, w, bias, y, ws, stream, prof); break;
         default: e = cudaErrorInvalidValue; break;
     }
     if (owned) {
@@ -316,12 +316,14 @@ int ct_conv_transpose_workspace_bytes(int nd, int64_t B, int64_t C_in, int64_t C
                                                    groups, dtype, CT_ROUTE_AUTO, bytes);
 }
 
-int ct_conv_transpose_nd_route(const void* x, const void* w, const void* bias, void* y,
-                               void* workspace, size_t workspace_bytes, int nd, int64_t B,
-                               int64_t C_in, int64_t C_out, const int64_t* in_spatial,
-                               const int64_t* k, const int* stride, const int* pad_lo,
-                               const int* pad_hi, const int* dilation, const int* output_padding,
-                               int groups, int dtype, int route, void* stream) {
+int ct_conv_transpose_nd_profiled(const void* x, const void* w, const void* bias, void* y,
+                                  void* workspace, size_t workspace_bytes, int nd, int64_t B,
+                                  int64_t C_in, int64_t C_out, const int64_t* in_spatial,
+                                  const int64_t* k, const int* stride, const int* pad_lo,
+                                  const int* pad_hi, const int* dilation,
+                                  const int* output_padding, int groups, int dtype, int route,
+                                  void* stream, void* main_start, void* main_stop, int* launches,
+                                  int* route_taken) {
     Problem p;
     int rc = validate(&p, nd, B, C_in, C_out, in_spatial, k, stride, pad_lo, pad_hi, dilation,
                       output_padding, groups, dtype);
@@ -333,7 +335,25 @@ int ct_conv_transpose_nd_route(const void* x, const void* w, const void* bias, v
     } else if (!route_supports(p, route)) {
         return fail(CT_ERR_ROUTE, "route %d cannot run this problem", route);
     }
-    return run(p, route, x, w, bias, y, workspace, workspace_bytes, (cudaStream_t)stream);
+    Profile prof;
+    prof.main_start = (cudaEvent_t)main_start;
+    prof.main_stop = (cudaEvent_t)main_stop;
+    rc = run(p, route, x, w, bias, y, workspace, workspace_bytes, (cudaStream_t)stream, &prof);
+    if (launches) *launches = prof.launches;
+    if (route_taken) *route_taken = route;
+    return rc;
+}
+
+int ct_conv_transpose_nd_route(const void* x, const void* w, const void* bias, void* y,
+                               void* workspace, size_t workspace_bytes, int nd, int64_t B,
+                               int64_t C_in, int64_t C_out, const int64_t* in_spatial,
+                               const int64_t* k, const int* stride, const int* pad_lo,
+                               const int* pad_hi, const int* dilation, const int* output_padding,
+                               int groups, int dtype, int route, void* stream) {
+    return ct_conv_transpose_nd_profiled(x, w, bias, y, workspace, workspace_bytes, nd, B, C_in,
+                                         C_out, in_spatial, k, stride, pad_lo, pad_hi, dilation,
+                                         output_padding, groups, dtype, route, stream, nullptr,
+                                         nullptr, nullptr, nullptr);
 }
 
 int ct_conv_transpose_nd(const void* x, const void* w, const void* bias, void* y, void* workspace,

@@ -131,7 +131,7 @@ __global__ void bias_fill_kernel(const T* __restrict__ bias, T* __restrict__ y, 
 
 template <typename T, int OCB>
 cudaError_t launch_gather_t(const GatherArgs& a, cudaStream_t stream, int sm_count,
-                            size_t smem_optin) {
+                            size_t smem_optin, Profile* prof) {
     const size_t slab = (size_t)a.Kn * a.Cig * OCB * sizeof(float);
     const bool use_smem = slab <= 48 * 1024 || slab <= smem_optin / 2;
     const int threads = 128;
@@ -150,15 +150,20 @@ cudaError_t launch_gather_t(const GatherArgs& a, cudaStream_t stream, int sm_cou
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)slab);
             if (e != cudaSuccess) return e;
         }
+        prof_begin(prof, stream);
         gather_kernel<T, OCB, true><<<grid, threads, slab, stream>>>(a);
     } else {
+        prof_begin(prof, stream);
         gather_kernel<T, OCB, false><<<grid, threads, 0, stream>>>(a);
     }
+    prof_end(prof, stream);
+    prof_count(prof);
     return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t launch_gather_dtype(const Problem& p, GatherArgs a, cudaStream_t stream) {
+cudaError_t launch_gather_dtype(const Problem& p, GatherArgs a, cudaStream_t stream,
+                                Profile* prof) {
     DeviceInfo d;
     cudaError_t e = device_info(&d);
     if (e != cudaSuccess) return e;
@@ -170,18 +175,18 @@ cudaError_t launch_gather_dtype(const Problem& p, GatherArgs a, cudaStream_t str
     a.n_ocb = (p.Cog + ocb - 1) / ocb;
     a.n_rows = p.B * (int64_t)p.G * a.n_ocb;
     switch (ocb) {
-        case 1: return launch_gather_t<T, 1>(a, stream, d.sm_count, d.smem_optin);
-        case 2: return launch_gather_t<T, 2>(a, stream, d.sm_count, d.smem_optin);
-        case 4: return launch_gather_t<T, 4>(a, stream, d.sm_count, d.smem_optin);
-        case 8: return launch_gather_t<T, 8>(a, stream, d.sm_count, d.smem_optin);
-        default: return launch_gather_t<T, 16>(a, stream, d.sm_count, d.smem_optin);
+        case 1: return launch_gather_t<T, 1>(a, stream, d.sm_count, d.smem_optin, prof);
+        case 2: return launch_gather_t<T, 2>(a, stream, d.sm_count, d.smem_optin, prof);
+        case 4: return launch_gather_t<T, 4>(a, stream, d.sm_count, d.smem_optin, prof);
+        case 8: return launch_gather_t<T, 8>(a, stream, d.sm_count, d.smem_optin, prof);
+        default: return launch_gather_t<T, 16>(a, stream, d.sm_count, d.smem_optin, prof);
     }
 }
 
 }  // namespace
 
 cudaError_t launch_gather(const Problem& p, const void* x, const void* w, const void* bias, void* y,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, Profile* prof) {
     GatherArgs a{};
     a.x = x; a.w = w; a.bias = bias; a.y = y;
     a.C_in = p.C_in; a.C_out = p.C_out;
@@ -194,13 +199,14 @@ cudaError_t launch_gather(const Problem& p, const void* x, const void* w, const 
     a.On = p.out_spatial();
     a.Kn = (int)p.taps();
     switch (p.dtype) {
-        case CT_F32: return launch_gather_dtype<float>(p, a, stream);
-        case CT_F16: return launch_gather_dtype<__half>(p, a, stream);
-        default: return launch_gather_dtype<__nv_bfloat16>(p, a, stream);
+        case CT_F32: return launch_gather_dtype<float>(p, a, stream, prof);
+        case CT_F16: return launch_gather_dtype<__half>(p, a, stream, prof);
+        default: return launch_gather_dtype<__nv_bfloat16>(p, a, stream, prof);
     }
 }
 
-cudaError_t launch_bias_fill(const Problem& p, const void* bias, void* y, cudaStream_t stream) {
+cudaError_t launch_bias_fill(const Problem& p, const void* bias, void* y, cudaStream_t stream,
+                             Profile* prof) {
     const int64_t total = p.y_elems();
     if (total == 0) return cudaSuccess;
     DeviceInfo d;
@@ -210,6 +216,7 @@ cudaError_t launch_bias_fill(const Problem& p, const void* bias, void* y, cudaSt
     int64_t blocks = (total + threads - 1) / threads;
     blocks = std::min<int64_t>(blocks, (int64_t)d.sm_count * 8);
     const int64_t On = p.out_spatial();
+    prof_begin(prof, stream);
     switch (p.dtype) {
         case CT_F32:
             bias_fill_kernel<float><<<(unsigned)blocks, threads, 0, stream>>>(
@@ -224,6 +231,8 @@ cudaError_t launch_bias_fill(const Problem& p, const void* bias, void* y, cudaSt
                 (const __nv_bfloat16*)bias, (__nv_bfloat16*)y, p.C_out, On, total);
             break;
     }
+    prof_end(prof, stream);
+    prof_count(prof);
     return cudaGetLastError();
 }
 

@@ -59,10 +59,30 @@ struct DeviceInfo {
 };
 cudaError_t device_info(DeviceInfo* out);
 
+// Optional per-call profiling: events recorded on the launching stream just
+// before and just after the route's dominant kernel, and a count of the
+// kernels the call launched.
+struct Profile {
+    cudaEvent_t main_start = nullptr;
+    cudaEvent_t main_stop = nullptr;
+    int launches = 0;
+};
+
+// Brackets the dominant kernel's launch with the profile events (if any).
+inline void prof_begin(Profile* pr, cudaStream_t s) {
+    if (pr && pr->main_start) cudaEventRecord(pr->main_start, s);
+}
+inline void prof_end(Profile* pr, cudaStream_t s) {
+    if (pr && pr->main_stop) cudaEventRecord(pr->main_stop, s);
+}
+inline void prof_count(Profile* pr, int n = 1) {
+    if (pr) pr->launches += n;
+}
+
 // Launchers.  Each returns the first CUDA error it met (cudaSuccess if none).
 cudaError_t launch_bias_fill(const Problem& p, const void* bias, void* y,
-                             cudaStream_t stream);
+                             cudaStream_t stream, Profile* prof);
 cudaError_t launch_gather(const Problem& p, const void* x, const void* w,
-                          const void* bias, void* y, cudaStream_t stream);
+                          const void* bias, void* y, cudaStream_t stream, Profile* prof);
 
 }  // namespace ct

@@ -10,20 +10,20 @@ namespace ct {
 bool grouped_supports(const Problem& p);
 bool grouped_preferred(const Problem& p);
 cudaError_t launch_grouped(const Problem& p, const void* x, const void* w, const void* bias,
-                           void* y, cudaStream_t stream);
+                           void* y, cudaStream_t stream, Profile* prof);
 
 // fp32 stride-phase implicit GEMM on CUDA cores (ct_simt.cu).
 bool simt_supports(const Problem& p);
 bool simt_preferred(const Problem& p);
 size_t simt_workspace_bytes(const Problem& p);
 cudaError_t launch_simt(const Problem& p, const void* x, const void* w, const void* bias, void* y,
-                        void* workspace, cudaStream_t stream);
+                        void* workspace, cudaStream_t stream, Profile* prof);
 
 // bf16/fp16 stride-phase implicit GEMM on tcgen05 tensor cores (ct_tc.cu).
 bool tc_supports(const Problem& p);
 bool tc_preferred(const Problem& p);
 size_t tc_workspace_bytes(const Problem& p);
 cudaError_t launch_tc(const Problem& p, const void* x, const void* w, const void* bias, void* y,
-                      void* workspace, cudaStream_t stream);
+                      void* workspace, cudaStream_t stream, Profile* prof);
 
 }  // namespace ct

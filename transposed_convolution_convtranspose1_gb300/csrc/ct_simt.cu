@@ -7,7 +7,7 @@ bool simt_supports(const Problem&) { return false; }
 bool simt_preferred(const Problem&) { return false; }
 size_t simt_workspace_bytes(const Problem&) { return 0; }
 cudaError_t launch_simt(const Problem&, const void*, const void*, const void*, void*, void*,
-                        cudaStream_t) {
+                        cudaStream_t, Profile*) {
     return cudaErrorNotSupported;
 }
 

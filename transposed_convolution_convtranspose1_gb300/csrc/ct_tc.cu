@@ -10,7 +10,7 @@ bool tc_supports(const Problem&) { return false; }
 bool tc_preferred(const Problem&) { return false; }
 size_t tc_workspace_bytes(const Problem&) { return 0; }
 cudaError_t launch_tc(const Problem&, const void*, const void*, const void*, void*, void*,
-                      cudaStream_t) {
+                      cudaStream_t, Profile*) {
     return cudaErrorNotSupported;
 }
 

@@ -46,7 +46,8 @@ EXPORTS = ("ct_version", "ct_last_error", "ct_status_string",
            "ct_conv_transpose_out_shape", "ct_conv_transpose_workspace_bytes",
            "ct_conv_transpose_route", "ct_conv_transpose_route_workspace_bytes",
            "ct_conv_transpose_nd", "ct_conv_transpose_nd_route",
-           "ct_conv_transpose_nd_host", "ct_device_status")
+           "ct_conv_transpose_nd_host", "ct_conv_transpose_nd_profiled",
+           "ct_device_status")
 
 
 class CtError(RuntimeError):
@@ -91,6 +92,10 @@ def _declare(h):
     h.ct_conv_transpose_nd_route.restype = ctypes.c_int
     h.ct_conv_transpose_nd_route.argtypes = ([_vp, _vp, _vp, _vp, _vp, ctypes.c_size_t]
                                              + _SHAPE_ARGS + [ctypes.c_int, _vp])
+    h.ct_conv_transpose_nd_profiled.restype = ctypes.c_int
+    h.ct_conv_transpose_nd_profiled.argtypes = ([_vp, _vp, _vp, _vp, _vp, ctypes.c_size_t]
+                                                + _SHAPE_ARGS + [ctypes.c_int, _vp, _vp, _vp,
+                                                                 _i32p, _i32p])
     h.ct_conv_transpose_nd_host.restype = ctypes.c_int
     h.ct_conv_transpose_nd_host.argtypes = [_vp, _vp, _vp, _vp] + _SHAPE_ARGS + [_vp]
     h.ct_device_status.restype = ctypes.c_int
@@ -248,6 +253,29 @@ def ct_conv_transpose_nd(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.
     else:
         rc = lib().ct_conv_transpose_nd_route(*args, int(route), s)
     _check(rc)
+
+
+def ct_conv_transpose_nd_profiled(x, w, bias, y, workspace=None, stride=None, pad_lo=None,
+                                  pad_hi=None, dilation=None, output_padding=None, groups=1,
+                                  route=CT_ROUTE_AUTO, stream=None, main_start=None,
+                                  main_stop=None):
+    """Device entry point with events around the dominant kernel.
+
+    main_start / main_stop are torch.cuda.Event objects (recorded at least once
+    before, so that their handles exist) or None.  Returns (launches, route).
+    """
+    nd, B, C_in, C_out, I, K = _problem_from_tensors(x, w, groups)
+    ax = _Axes(nd, I, K, stride, pad_lo, pad_hi, dilation, output_padding)
+    s = _stream_handle(stream, x.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    n = ctypes.c_int(0)
+    r = ctypes.c_int(-1)
+    ev = lambda e: None if e is None else e.cuda_event
+    _check(lib().ct_conv_transpose_nd_profiled(
+        _ptr(x), _ptr(w), _ptr(bias), _ptr(y), _ptr(workspace), ws_bytes,
+        *_shape_args(B, C_in, C_out, ax, groups, dtype_code(x.dtype)), int(route), s,
+        ev(main_start), ev(main_stop), ctypes.byref(n), ctypes.byref(r)))
+    return int(n.value), int(r.value)
 
 
 def ct_conv_transpose_nd_host(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
