@@ -1,17 +1,779 @@
-// ct_tc.cu -- tensor-core (tcgen05) stride-phase implicit GEMM route.
+// ct_tc.cu -- bf16/fp16 stride-phase implicit GEMM on tcgen05 tensor cores.
+//
+// Method.  Output positions are split by their residue r_a = o_a mod s_a on
+// every axis (stride phases).  Within a phase every output o = r + s*q
+// receives the same set of taps T_r, each reading input i = q + off(r, t), so
+// the phase is a dense GEMM
+//     Y_r[b, q, oc] = sum_{t in T_r, ic} X[b, q + off(r,t), ic] * W[t][oc][ic]
+// over C_in x |T_r| -- the ONNX page's implicit-gather GEMM with tap-reversed
+// weights (ai.onnx.ConvTranspose, variant ncdhw3d_implicit_sgmat: no column
+// matrix, no scatter pass, reduction over the full in-channel-by-tap depth),
+// generalised from stride 1 to every stride phase.  Three kernels run:
+//   1. tc_weight_reorder : w [C_in, C_out, taps] -> W' [taps][N_pad][C_pad]
+//                          (K-major B operand, zero padded; taps indexed in the
+//                          pages' unflipped order, visited per phase in
+//                          reversed order, i.e. increasing input offset)
+//   2. tc_channels_last  : x [B, C, D*H*W] -> X' [B, D, H, W, C_pad]
+//                          (K-major A operand; TMA boxes then shift along the
+//                          spatial axes only, so every box starts on a
+//                          128-byte boundary of the channel axis)
+//   3. tc_phase_gemm     : persistent, warp-specialised:
+//        warp 0      TMA producer: per k-block one 5-D box of X' shifted by
+//                    the tap's input offset (out-of-range rows zero-filled by
+//                    TMA) and one box of W', into a ring of SW128 stages
+//        warp 1      TMEM allocator and single-thread tcgen05.mma issuer,
+//                    M = 128 output positions, N = output-channel tile,
+//                    K = 16 per instruction, fp32 accumulators in TMEM
+//        warps 2..5  epilogue: tcgen05.ld, + bias in fp32, one RNE rounding,
+//                    stores interleaving the W phases of a tile so that a warp
+//                    writes whole output rows
+//      A tile holds every W phase of its positions (one accumulator each);
+//      accumulators are double-buffered so the epilogue of one tile overlaps
+//      the MMAs of the next.  Every mbarrier wait is bounded: on time-out the
+//      kernel records a code in g_device_error, stops issuing work, drains
+//      its outstanding copies and MMAs (bounded too), frees TMEM and returns.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "ct_routes.h"
+#include "ct_types.cuh"
 
 namespace ct {
 
 // Error word written by bounded device-side waits (0 = none).
 __device__ unsigned int g_device_error = 0;
 
-bool tc_supports(const Problem&) { return false; }
-bool tc_preferred(const Problem&) { return false; }
-size_t tc_workspace_bytes(const Problem&) { return 0; }
-cudaError_t launch_tc(const Problem&, const void*, const void*, const void*, void*, void*,
-                      cudaStream_t, Profile*) {
-    return cudaErrorNotSupported;
+namespace {
+
+constexpr int kTcMaxS = 8;        // stride per axis on this route
+constexpr int kTcMaxTaps = 8;     // taps per axis and phase on this route
+constexpr int kTcMaxClasses = 32; // (D residue, H residue) classes
+constexpr int kBlockM = 128;      // output positions per tile (TMEM lanes)
+constexpr int kBlockK = 64;       // channels per k-block (one 128-byte row)
+constexpr int kThreads = 192;     // 6 warps
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait before giving up
+
+// Error codes in g_device_error (bit flags).
+constexpr unsigned kErrProducer = 1u << 0;
+constexpr unsigned kErrMma = 1u << 1;
+constexpr unsigned kErrEpilogue = 1u << 2;
+constexpr unsigned kErrDrain = 1u << 3;
+
+struct TcClass {
+    int rd, rh;           // D and H residues
+    int start, count;     // tile index range
+    int n_qd, n_qh_blk, n_qw_blk;
+    int qd_ext, qh_ext;   // q extents of this class on D and H
+};
+
+struct TcParams {
+    CUtensorMap tmap_a;   // X' [B, D, H, W, C_pad] as 5-D (C_pad, W, H, D, B)
+    CUtensorMap tmap_b;   // W' [taps][N_pad][C_pad] as 3-D (C_pad, N_pad, taps)
+    const void* bias;
+    void* y;
+    int C_out, n_kblk, n_tile, n_oc_tiles;
+    int O[3];
+    int S[3];
+    int Kdims[3];         // kD, kH, kW (for the flat tap index)
+    int WC, MR;           // tile = MR rows of WC positions along W
+    int sw;               // W stride = number of W phases per tile
+    int qw_ext[kTcMaxS];  // q extent of each W residue
+    int ntap[3][kTcMaxS];
+    int tap[3][kTcMaxS][kTcMaxTaps];
+    int off[3][kTcMaxS][kTcMaxTaps];
+    int n_classes, total_tiles;
+    TcClass cls[kTcMaxClasses];
+    int stages;
+    uint32_t stage_bytes, a_bytes;
+    uint32_t idesc;
+    uint32_t tmem_cols;
+    int acc_stride;       // TMEM columns per accumulator buffer (sw * n_tile)
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false when the wait ran past
+// kWaitNs (after recording `code` in g_device_error and raising *abort) or
+// when another role has already given up (*abort set).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned code,
+                                          volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > kWaitNs) {
+                if (code) atomicOr(&g_device_error, code);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait used while draining after an abort (no new error recorded).
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > kWaitNs) {
+            atomicOr(&g_device_error, kErrDrain);
+            return;
+        }
+}
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+        "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, rows of 128
+// bytes, 8-row groups 1024 bytes apart (SBO), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);       // start address
+    d |= (uint64_t)(16u >> 4) << 16;               // leading byte offset (unused here)
+    d |= (uint64_t)(1024u >> 4) << 32;             // stride byte offset
+    d |= (uint64_t)1 << 46;                        // version
+    d |= (uint64_t)2 << 61;                        // SWIZZLE_128B
+    return d;
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tile decode (identical in every role)
+// ---------------------------------------------------------------------------
+
+struct Tile {
+    int cls, rd, rh, b, qd, qh0, qw0, oc0;
+};
+
+__device__ __forceinline__ Tile decode_tile(const TcParams& P, int t) {
+    const TcClass* cls = P.cls;
+    int c = 0;
+    while (c + 1 < P.n_classes && t >= cls[c + 1].start) ++c;
+    const TcClass& C = cls[c];
+    int local = t - C.start;
+    Tile T;
+    T.cls = c;
+    T.rd = C.rd;
+    T.rh = C.rh;
+    const int oc_t = local % P.n_oc_tiles; local /= P.n_oc_tiles;
+    const int qw_b = local % C.n_qw_blk; local /= C.n_qw_blk;
+    const int qh_b = local % C.n_qh_blk; local /= C.n_qh_blk;
+    T.qd = local % C.n_qd;
+    T.b = local / C.n_qd;
+    T.qh0 = qh_b * P.MR;
+    T.qw0 = qw_b * P.WC;
+    T.oc0 = oc_t * P.n_tile;
+    return T;
+}
+
+__device__ __forceinline__ int phase_taps(const TcParams& P, const Tile& T, int rw) {
+    return P.ntap[0][T.rd] * P.ntap[1][T.rh] * P.ntap[2][rw];
+}
+
+__device__ __forceinline__ bool tile_has_work(const TcParams& P, const Tile& T) {
+    for (int rw = 0; rw < P.sw; ++rw)
+        if (phase_taps(P, T, rw) > 0) return true;
+    return false;
+}
+
+// ---------------------------------------------------------------------------
+// the GEMM kernel
+// ---------------------------------------------------------------------------
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_constant__ TcParams P) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint64_t full_bar[16], empty_bar[16], tfull_bar[2], tempty_bar[2], drain_bar;
+    __shared__ uint32_t tmem_base_slot;
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    // 1024-byte aligned stage ring (SW128 atoms need the alignment)
+    const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < P.stages; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&tfull_bar[b]), 1);
+            mbar_init(smem_u32(&tempty_bar[b]), 128);
+        }
+        mbar_init(smem_u32(&drain_bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_a))
+                     : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_b))
+                     : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&tmem_base_slot)),
+                     "r"(P.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_base_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        // The whole warp walks the schedule; lane 0 issues the copies.
+        uint32_t kiter = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+            const Tile tl = decode_tile(P, t);
+            for (int rw = 0; rw < P.sw && ok; ++rw) {
+                const int nd_ = P.ntap[0][tl.rd], nh_ = P.ntap[1][tl.rh], nw_ = P.ntap[2][rw];
+                for (int jd = 0; jd < nd_ && ok; ++jd)
+                    for (int jh = 0; jh < nh_ && ok; ++jh)
+                        for (int jw = 0; jw < nw_ && ok; ++jw) {
+                            const int tap = (P.tap[0][tl.rd][jd] * P.Kdims[1] + P.tap[1][tl.rh][jh]) *
+                                                P.Kdims[2] +
+                                            P.tap[2][rw][jw];
+                            const int id = tl.qd + P.off[0][tl.rd][jd];
+                            const int ih = tl.qh0 + P.off[1][tl.rh][jh];
+                            const int iw = tl.qw0 + P.off[2][rw][jw];
+                            for (int kb = 0; kb < P.n_kblk; ++kb) {
+                                const int s = kiter % P.stages;
+                                const uint32_t par = ((kiter / P.stages) & 1) ^ 1;
+                                ok = __all_sync(0xffffffffu,
+                                                mbar_wait(smem_u32(&empty_bar[s]), par,
+                                                          kErrProducer, &abort_flag));
+                                if (!ok) break;
+                                if (lane == 0) {
+                                    const uint32_t fb = smem_u32(&full_bar[s]);
+                                    const uint32_t sa = ring + s * P.stage_bytes;
+                                    mbar_expect_tx(fb, P.stage_bytes);
+                                    tma_load_5d(sa, &P.tmap_a, fb, kb * kBlockK, iw, ih, id, tl.b);
+                                    tma_load_3d(sa + P.a_bytes, &P.tmap_b, fb, kb * kBlockK, tl.oc0,
+                                                tap);
+                                }
+                                __syncwarp();
+                                ++kiter;
+                            }
+                        }
+            }
+        }
+        if (!ok && lane == 0) {
+            // every copy issued so far must land before the CTA exits
+            const uint32_t first = kiter > (uint32_t)P.stages ? kiter - P.stages : 0;
+            for (uint32_t k = first; k < kiter; ++k)
+                mbar_drain(smem_u32(&full_bar[k % P.stages]), (k / P.stages) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        // The whole warp walks the schedule; lane 0 issues MMAs and commits.
+        uint32_t kiter = 0, acc_iter = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+            const Tile tl = decode_tile(P, t);
+            if (!tile_has_work(P, tl)) continue;
+            const int buf = acc_iter & 1;
+            const uint32_t tpar = ((acc_iter >> 1) & 1) ^ 1;
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(smem_u32(&tempty_bar[buf]), tpar, kErrMma, &abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            for (int rw = 0; rw < P.sw && ok; ++rw) {
+                const int nk = phase_taps(P, tl, rw) * P.n_kblk;
+                const uint32_t d = tmem_base + buf * P.acc_stride + rw * P.n_tile;
+                for (int j = 0; j < nk; ++j) {
+                    const int s = kiter % P.stages;
+                    const uint32_t par = (kiter / P.stages) & 1;
+                    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[s]), par, kErrMma,
+                                                           &abort_flag));
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t sa = ring + s * P.stage_bytes;
+                        const uint64_t ad = smem_desc_sw128(sa);
+                        const uint64_t bd = smem_desc_sw128(sa + P.a_bytes);
+#pragma unroll
+                        for (int k = 0; k < kBlockK / 16; ++k) {
+                            // advance along K by 16 elements = 32 bytes (encoded >> 4: 2)
+                            mma_f16(d, ad + 2 * k, bd + 2 * k, P.idesc,
+                                    (j > 0 || k > 0) ? 1u : 0u);
+                        }
+                        mma_commit(smem_u32(&empty_bar[s]));
+                    }
+                    __syncwarp();
+                    ++kiter;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) mma_commit(smem_u32(&tfull_bar[buf]));
+            __syncwarp();
+            ++acc_iter;
+        }
+        // no MMA may be in flight when TMEM is released
+        if (lane == 0) {
+            mma_commit(smem_u32(&drain_bar));
+            mbar_drain(smem_u32(&drain_bar), 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;             // TMEM lane quarter this warp may access
+        const int m = q * 32 + lane;        // tile row = output position
+        const int row = m / P.WC, col = m % P.WC;
+        const T* __restrict__ bias = static_cast<const T*>(P.bias);
+        T* __restrict__ y = static_cast<T*>(P.y);
+        const int64_t chan_rows = (int64_t)P.O[0] * P.O[1];  // output rows per channel
+        uint32_t acc_iter = 0;
+        for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x) {
+            const Tile Tl = decode_tile(P, t);
+            const TcClass& C = P.cls[Tl.cls];
+            const bool work = tile_has_work(P, Tl);
+            const int buf = acc_iter & 1;
+            if (work) {
+                const bool ok = __all_sync(
+                    0xffffffffu, mbar_wait(smem_u32(&tfull_bar[buf]), (acc_iter >> 1) & 1,
+                                           kErrEpilogue, &abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+            }
+            const int qh = Tl.qh0 + row, qw = Tl.qw0 + col;
+            const bool pos_ok = (Tl.qd < C.qd_ext) && (qh < C.qh_ext);
+            const int od = Tl.rd + P.S[0] * Tl.qd;
+            const int oh = Tl.rh + P.S[1] * qh;
+            // index of output row (b, oc = 0, od, oh)
+            const int64_t row0 = ((int64_t)Tl.b * P.C_out * P.O[0] + od) * P.O[1] + oh;
+            for (int j0 = 0; j0 < P.n_tile; j0 += 16) {
+                float bv[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int oc = Tl.oc0 + j0 + i;
+                    bv[i] = (bias != nullptr && oc < P.C_out) ? to_f32(bias[oc]) : 0.f;
+                }
+                for (int rw = 0; rw < P.sw; ++rw) {
+                    float v[16];
+                    if (work && phase_taps(P, Tl, rw) > 0) {
+                        tmem_ld16(tmem_base + ((uint32_t)(q * 32) << 16) +
+                                      (uint32_t)(buf * P.acc_stride + rw * P.n_tile + j0),
+                                  v);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                    }
+                    const int ow = rw + P.sw * qw;
+                    if (pos_ok && qw < P.qw_ext[rw]) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int oc = Tl.oc0 + j0 + i;
+                            if (oc < P.C_out)
+                                y[(row0 + (int64_t)oc * chan_rows) * P.O[2] + ow] =
+                                    from_f32<T>(v[i] + bv[i]);
+                        }
+                    }
+                }
+            }
+            if (work) {
+                tc_fence_before();
+                mbar_arrive(smem_u32(&tempty_bar[buf]));
+                ++acc_iter;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(P.tmem_cols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
+// layout kernels
+// ---------------------------------------------------------------------------
+
+// W'[tap][n][c] = w[c][n][tap] for n < C_out, c < C_in, else 0.
+template <typename T>
+__global__ void tc_weight_reorder(const T* __restrict__ w, T* __restrict__ wp, int C_in, int C_out,
+                                  int taps, int N_pad, int C_pad) {
+    const int64_t total = (int64_t)taps * N_pad * C_pad;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int c = (int)(e % C_pad);
+        const int n = (int)((e / C_pad) % N_pad);
+        const int t = (int)(e / ((int64_t)C_pad * N_pad));
+        T v = from_f32<T>(0.f);
+        if (c < C_in && n < C_out) v = w[((int64_t)c * C_out + n) * taps + t];
+        wp[e] = v;
+    }
+}
+
+// X'[b][s][c] = x[b][c][s] for c < C, 0 for C <= c < C_pad.  64 x 64 tiles
+// through shared memory: reads are coalesced along s, writes along c.
+template <typename T>
+__global__ void __launch_bounds__(256) tc_channels_last(const T* __restrict__ x, T* __restrict__ xc,
+                                                        int C, int C_pad, int64_t S) {
+    __shared__ uint16_t tile[64][66];
+    const int64_t s0 = (int64_t)blockIdx.x * 64;
+    const int c0 = blockIdx.y * 64;
+    const int64_t b = blockIdx.z;
+    const int tx = threadIdx.x % 64, ty = threadIdx.x / 64;
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(x);
+    uint16_t* xd = reinterpret_cast<uint16_t*>(xc);
+    for (int c = ty; c < 64; c += 4) {
+        uint16_t v = 0;
+        const int64_t s = s0 + tx;
+        if (c0 + c < C && s < S) v = xs[(b * C + c0 + c) * S + s];
+        tile[c][tx] = v;
+    }
+    __syncthreads();
+    for (int s = ty; s < 64; s += 4) {
+        const int64_t ss = s0 + s;
+        if (ss < S) xd[(b * S + ss) * C_pad + c0 + tx] = tile[tx][s];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host planning
+// ---------------------------------------------------------------------------
+
+struct TcPlan {
+    int C_pad, N_pad, n_tile, n_oc_tiles, sw, WC, MR, stages;
+    size_t x_bytes, w_bytes;
+    AxisPlan ax[3];
+};
+
+bool make_plan(const Problem& p, TcPlan* pl) {
+    if (p.dtype != CT_BF16 && p.dtype != CT_F16) return false;
+    if (p.G != 1) return false;
+    for (int a = 0; a < 3; ++a) {
+        if (p.S[a] > kTcMaxS) return false;
+        plan_axis(p, a, &pl->ax[a]);
+        for (int r = 0; r < p.S[a]; ++r)
+            if (pl->ax[a].ntaps[r] > kTcMaxTaps) return false;
+    }
+    if (p.S[0] * p.S[1] > kTcMaxClasses) return false;
+    pl->sw = p.S[2];
+    int nt = (int)((256 / pl->sw) / 16) * 16;  // two accumulator buffers in 512 columns
+    if (nt < 16) return false;
+    const int cout16 = (int)((p.C_out + 15) / 16 * 16);
+    pl->n_tile = std::min(std::min(nt, 256), cout16);
+    pl->n_oc_tiles = (int)((p.C_out + pl->n_tile - 1) / pl->n_tile);
+    pl->N_pad = pl->n_oc_tiles * pl->n_tile;
+    pl->C_pad = (int)((p.C_in + kBlockK - 1) / kBlockK * kBlockK);
+    const int64_t qw0 = pl->ax[2].q_extent[0];
+    int wc = 8;
+    while (wc < qw0 && wc < 128) wc *= 2;
+    pl->WC = wc;
+    pl->MR = kBlockM / wc;
+    const size_t stage = (size_t)kBlockM * 128 + (size_t)pl->n_tile * 128;
+    pl->stages = (int)std::min<size_t>(8, (227 * 1024 - 2048) / stage);
+    if (pl->stages < 2) return false;
+    pl->x_bytes = (size_t)p.B * p.in_spatial() * pl->C_pad * 2;
+    pl->w_bytes = (size_t)p.taps() * pl->N_pad * pl->C_pad * 2;
+    // TMA limits: every global extent < 2^32, strides < 2^40
+    if (p.in_spatial() * (int64_t)pl->C_pad * 2 * p.B >= (1ll << 40)) return false;
+    return true;
+}
+
+size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+template <typename T>
+cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const void* w,
+                        const void* bias, void* y, void* workspace, cudaStream_t stream,
+                        Profile* prof) {
+    DeviceInfo dev;
+    cudaError_t e = device_info(&dev);
+    if (e != cudaSuccess) return e;
+    char* ws = static_cast<char*>(workspace);
+    T* xc = reinterpret_cast<T*>(ws);
+    T* wp = reinterpret_cast<T*>(ws + round256(pl.x_bytes));
+
+    // ---- parameters
+    TcParams P;
+    std::memset(&P, 0, sizeof(P));
+    P.bias = bias;
+    P.y = y;
+    P.C_out = (int)p.C_out;
+    P.n_kblk = pl.C_pad / kBlockK;
+    P.n_tile = pl.n_tile;
+    P.n_oc_tiles = pl.n_oc_tiles;
+    for (int a = 0; a < 3; ++a) {
+        P.O[a] = (int)p.O[a];
+        P.S[a] = p.S[a];
+        P.Kdims[a] = (int)p.K[a];
+        for (int r = 0; r < p.S[a]; ++r) {
+            P.ntap[a][r] = pl.ax[a].ntaps[r];
+            for (int j = 0; j < pl.ax[a].ntaps[r]; ++j) {
+                P.tap[a][r][j] = pl.ax[a].tap[r][j];
+                P.off[a][r][j] = pl.ax[a].off[r][j];
+            }
+        }
+    }
+    P.WC = pl.WC;
+    P.MR = pl.MR;
+    P.sw = pl.sw;
+    for (int r = 0; r < pl.sw; ++r) P.qw_ext[r] = (int)pl.ax[2].q_extent[r];
+    P.stages = pl.stages;
+    P.a_bytes = kBlockM * 128;
+    P.stage_bytes = P.a_bytes + pl.n_tile * 128;
+    P.acc_stride = pl.sw * pl.n_tile;
+    uint32_t cols = 32;
+    while (cols < (uint32_t)(2 * P.acc_stride)) cols *= 2;
+    P.tmem_cols = cols;
+    P.idesc = (1u << 4)                                   // D = f32
+              | ((p.dtype == CT_BF16 ? 1u : 0u) << 7)     // A = bf16 / f16
+              | ((p.dtype == CT_BF16 ? 1u : 0u) << 10)    // B = bf16 / f16
+              | ((uint32_t)(pl.n_tile >> 3) << 17)        // N
+              | ((uint32_t)(kBlockM >> 4) << 24);         // M
+
+    // ---- tile classes, heaviest first (longest-processing-time order)
+    TcClass hc[kTcMaxClasses];
+    int work[kTcMaxClasses];
+    int n = 0;
+    const int qw_blk = (int)((pl.ax[2].q_extent[0] + pl.WC - 1) / pl.WC);
+    for (int rd = 0; rd < p.S[0]; ++rd)
+        for (int rh = 0; rh < p.S[1]; ++rh) {
+            const int64_t qd = pl.ax[0].q_extent[rd], qh = pl.ax[1].q_extent[rh];
+            if (qd == 0 || qh == 0 || qw_blk == 0) continue;
+            TcClass c{};
+            c.rd = rd;
+            c.rh = rh;
+            c.n_qd = (int)qd;
+            c.n_qh_blk = (int)((qh + pl.MR - 1) / pl.MR);
+            c.n_qw_blk = qw_blk;
+            c.qd_ext = (int)qd;
+            c.qh_ext = (int)qh;
+            c.count = (int)(p.B * c.n_qd * c.n_qh_blk * c.n_qw_blk * pl.n_oc_tiles);
+            int wsum = 0;
+            for (int rw = 0; rw < pl.sw; ++rw)
+                wsum += pl.ax[0].ntaps[rd] * pl.ax[1].ntaps[rh] * pl.ax[2].ntaps[rw];
+            work[n] = wsum;
+            hc[n++] = c;
+        }
+    for (int i = 0; i < n; ++i)  // stable selection sort, descending work
+        for (int j = i + 1; j < n; ++j)
+            if (work[j] > work[i]) {
+                std::swap(work[i], work[j]);
+                std::swap(hc[i], hc[j]);
+            }
+    int64_t total = 0;
+    for (int i = 0; i < n; ++i) {
+        hc[i].start = (int)total;
+        total += hc[i].count;
+    }
+    if (total >= (1ll << 31)) return cudaErrorInvalidValue;
+    P.n_classes = n;
+    P.total_tiles = (int)total;
+    for (int i = 0; i < n; ++i) P.cls[i] = hc[i];
+
+    // ---- tensor maps
+    auto enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const CUtensorMapDataType dt =
+        p.dtype == CT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    {
+        const cuuint64_t dims[5] = {(cuuint64_t)pl.C_pad, (cuuint64_t)p.I[2], (cuuint64_t)p.I[1],
+                                    (cuuint64_t)p.I[0], (cuuint64_t)p.B};
+        const cuuint64_t row = (cuuint64_t)pl.C_pad * 2;
+        const cuuint64_t strides[4] = {row, row * p.I[2], row * p.I[2] * p.I[1],
+                                       row * p.I[2] * p.I[1] * p.I[0]};
+        const cuuint32_t box[5] = {(cuuint32_t)kBlockK, (cuuint32_t)pl.WC, (cuuint32_t)pl.MR, 1, 1};
+        const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+        CUresult r = enc(&P.tmap_a, dt, 5, xc, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)pl.C_pad, (cuuint64_t)pl.N_pad,
+                                    (cuuint64_t)p.taps()};
+        const cuuint64_t strides[2] = {(cuuint64_t)pl.C_pad * 2,
+                                       (cuuint64_t)pl.C_pad * 2 * pl.N_pad};
+        const cuuint32_t box[3] = {(cuuint32_t)kBlockK, (cuuint32_t)pl.n_tile, 1};
+        const cuuint32_t es[3] = {1, 1, 1};
+        CUresult r = enc(&P.tmap_b, dt, 3, wp, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+
+    // ---- launches
+    {
+        const int64_t tot = p.taps() * pl.N_pad * pl.C_pad;
+        const int blocks = (int)std::min<int64_t>((tot + 255) / 256, (int64_t)dev.sm_count * 8);
+        tc_weight_reorder<T><<<blocks, 256, 0, stream>>>(static_cast<const T*>(w), wp, (int)p.C_in,
+                                                         (int)p.C_out, (int)p.taps(), pl.N_pad,
+                                                         pl.C_pad);
+        prof_count(prof);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    {
+        const int64_t S = p.in_spatial();
+        dim3 grid((unsigned)((S + 63) / 64), (unsigned)(pl.C_pad / 64), (unsigned)p.B);
+        if (grid.y > 65535 || grid.z > 65535) return cudaErrorInvalidConfiguration;
+        tc_channels_last<T><<<grid, 256, 0, stream>>>(static_cast<const T*>(x), xc, (int)p.C_in,
+                                                      pl.C_pad, S);
+        prof_count(prof);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    const size_t smem = (size_t)P.stages * P.stage_bytes + 1024;
+    e = cudaFuncSetAttribute(tc_phase_gemm<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    const int grid = std::max(1, std::min(P.total_tiles, dev.sm_count));
+    prof_begin(prof, stream);
+    tc_phase_gemm<T><<<grid, kThreads, smem, stream>>>(P);
+    prof_end(prof, stream);
+    prof_count(prof);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supports(const Problem& p) {
+    TcPlan pl;
+    if (!make_plan(p, &pl)) return false;
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess) return false;
+    return d.cc_major == 10 && d.cc_minor == 3;
+}
+
+bool tc_preferred(const Problem& p) { return p.C_in >= 16 && p.C_out >= 16; }
+
+size_t tc_workspace_bytes(const Problem& p) {
+    TcPlan pl;
+    if (!make_plan(p, &pl)) return 0;
+    return round256(pl.x_bytes) + round256(pl.w_bytes);
+}
+
+cudaError_t launch_tc(const Problem& p, const void* x, const void* w, const void* bias, void* y,
+                      void* workspace, cudaStream_t stream, Profile* prof) {
+    TcPlan pl;
+    if (!make_plan(p, &pl)) return cudaErrorInvalidValue;
+    if (p.dtype == CT_BF16)
+        return launch_tc_t<__nv_bfloat16>(p, pl, x, w, bias, y, workspace, stream, prof);
+    return launch_tc_t<__half>(p, pl, x, w, bias, y, workspace, stream, prof);
 }
 
 }  // namespace ct
