@@ -234,6 +234,43 @@ int ct_conv_transpose_nd_host(const void* x, const void* w, const void* bias,
                               int groups, int dtype, void* stream);
 
 /*
+ * Size of the fixed scratch array behind ct_conv_transpose_nd_noalloc.
+ */
+#define CT_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * Forward transposed convolution that allocates no device memory.  The pages
+ * have no counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc or cudaMallocAsync where they run the convolution -- code
+ * running under a CUDA graph capture that forbids allocation, inference-
+ * engine plugins that may only use memory the engine hands them, frameworks
+ * that own the whole device memory budget through their own pool, and
+ * real-time callers that allow no allocation after start-up.
+ *
+ * Arguments, layouts, validation and results are those of
+ * ct_conv_transpose_nd; x, w, bias and y are device pointers the caller owns.
+ * Instead of a workspace, the call uses one static device array of
+ * CT_NOALLOC_SCRATCH_BYTES (64 MiB) that every GPU which loads the library
+ * holds until the process exits.  A problem whose route needs more scratch
+ * than that is rejected with CT_ERR_WORKSPACE before any device work.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  All calls share the one array and
+ * it keeps whatever the last call left there; the kernels overwrite every
+ * byte of scratch they read, so no call depends on its contents.  Calls that
+ * may overlap on the GPU (different streams, or concurrent host threads on
+ * different streams) race on the array: serialise them.
+ */
+int ct_conv_transpose_nd_noalloc(const void* x, const void* w, const void* bias,
+                                 void* y, int nd, int64_t B, int64_t C_in,
+                                 int64_t C_out, const int64_t* in_spatial,
+                                 const int64_t* k, const int* stride,
+                                 const int* pad_lo, const int* pad_hi,
+                                 const int* dilation, const int* output_padding,
+                                 int groups, int dtype, void* stream);
+
+/*
  * Device-side error word written by bounded waits in the tensor-core kernel
  * (0 = none; otherwise the code says which wait gave up).  Synchronises the
  * current device, writes the word to *code and clears it when `clear` is

@@ -186,6 +186,14 @@ int check_pointers(const Problem& p, const void* x, const void* w, const void* b
 
 }  // namespace
 
+int report_error(int status, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
 void plan_axis(const Problem& p, int axis, AxisPlan* out) {
     const int s = p.S[axis];
     out->s = s;

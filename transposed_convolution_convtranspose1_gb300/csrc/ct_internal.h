@@ -50,6 +50,9 @@ struct AxisPlan {
 
 void plan_axis(const Problem& p, int axis, AxisPlan* out);
 
+// Records a message for ct_last_error() on this thread and returns `status`.
+int report_error(int status, const char* fmt, ...);
+
 // Device properties cached per device.
 struct DeviceInfo {
     int device;

@@ -47,7 +47,10 @@ EXPORTS = ("ct_version", "ct_last_error", "ct_status_string",
            "ct_conv_transpose_route", "ct_conv_transpose_route_workspace_bytes",
            "ct_conv_transpose_nd", "ct_conv_transpose_nd_route",
            "ct_conv_transpose_nd_host", "ct_conv_transpose_nd_profiled",
-           "ct_device_status")
+           "ct_conv_transpose_nd_noalloc", "ct_device_status")
+
+# Size of the static scratch behind ct_conv_transpose_nd_noalloc (CT_NOALLOC_SCRATCH_BYTES).
+CT_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class CtError(RuntimeError):
@@ -98,6 +101,8 @@ def _declare(h):
                                                                  _i32p, _i32p])
     h.ct_conv_transpose_nd_host.restype = ctypes.c_int
     h.ct_conv_transpose_nd_host.argtypes = [_vp, _vp, _vp, _vp] + _SHAPE_ARGS + [_vp]
+    h.ct_conv_transpose_nd_noalloc.restype = ctypes.c_int
+    h.ct_conv_transpose_nd_noalloc.argtypes = [_vp, _vp, _vp, _vp] + _SHAPE_ARGS + [_vp]
     h.ct_device_status.restype = ctypes.c_int
     h.ct_device_status.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_uint)]
 
@@ -289,6 +294,23 @@ def ct_conv_transpose_nd_host(x: torch.Tensor, w: torch.Tensor, bias: Optional[t
     ax = _Axes(nd, I, K, stride, pad_lo, pad_hi, dilation, output_padding)
     s = _stream_handle(stream, None)
     _check(lib().ct_conv_transpose_nd_host(
+        _ptr(x), _ptr(w), _ptr(bias), _ptr(y),
+        *_shape_args(B, C_in, C_out, ax, groups, dtype_code(x.dtype)), s))
+
+
+def ct_conv_transpose_nd_noalloc(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
+                                 y: torch.Tensor, stride=None, pad_lo=None, pad_hi=None,
+                                 dilation=None, output_padding=None, groups: int = 1,
+                                 stream=None) -> None:
+    """The entry point that allocates no device memory (for callers that may
+    not call cudaMalloc where they run the convolution).  It uses the
+    library's fixed static scratch; calls that overlap on the GPU race on it."""
+    nd, B, C_in, C_out, I, K = _problem_from_tensors(x, w, groups)
+    if bias is not None and tuple(bias.shape) != (C_out,):
+        raise CtError(CT_ERR_BIAS, f"bias must have shape [{C_out}], got {tuple(bias.shape)}")
+    ax = _Axes(nd, I, K, stride, pad_lo, pad_hi, dilation, output_padding)
+    s = _stream_handle(stream, x.device)
+    _check(lib().ct_conv_transpose_nd_noalloc(
         _ptr(x), _ptr(w), _ptr(bias), _ptr(y),
         *_shape_args(B, C_in, C_out, ax, groups, dtype_code(x.dtype)), s))
 
