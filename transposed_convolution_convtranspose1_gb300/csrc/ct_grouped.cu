@@ -1,13 +1,251 @@
 // ct_grouped.cu -- grouped/depthwise stride-phase gather on CUDA cores.
+//
+// The ONNX page's grouped stride-phase variant (ai.onnx.ConvTranspose,
+// nchw2d_grouped_stride_phase_blocked): one invocation owns output pixels and
+// the whole block of its group's output channels, every gathered input sample
+// feeds that block, and the group's weight slab is staged once per workgroup.
+// Laid out for GB300:
+//   - one warp per output row (b, od, oh), so every lane shares the row's D
+//     and H residues and therefore its tap lists (no divergence on them);
+//   - each lane owns one q along W and all s_w W residues of it, i.e. the s_w
+//     consecutive outputs s_w*q .. s_w*q + s_w - 1, so residues with no taps
+//     (bias only) and residues with taps sit in every lane alike;
+//   - accumulators for all COG output channels of the group in registers,
+//     weights read from the shared-memory slab as broadcasts, input samples
+//     read once per (tap, channel) with lanes on consecutive positions;
+//   - stores: for each output channel a warp writes 32*s_w consecutive
+//     elements of one output row.
+#include <algorithm>
+#include <cstring>
+
 #include "ct_routes.h"
+#include "ct_types.cuh"
 
 namespace ct {
+namespace {
 
-bool grouped_supports(const Problem&) { return false; }
-bool grouped_preferred(const Problem&) { return false; }
-cudaError_t launch_grouped(const Problem&, const void*, const void*, const void*, void*,
-                           cudaStream_t, Profile*) {
-    return cudaErrorNotSupported;
+constexpr int kGrpMaxS = 4;       // W stride handled by one lane
+constexpr int kGrpMaxSA = 8;      // D / H stride
+constexpr int kGrpMaxTaps = 8;    // taps per axis and residue
+constexpr int kGrpWarps = 8;      // rows per block
+constexpr size_t kGrpMaxSlab = 48 * 1024;
+
+struct GroupedParams {
+    const void* x;
+    const void* w;
+    const void* bias;
+    void* y;
+    int C_in, C_out, G, Cig, Cog;
+    int I[3], O[3], S[3], Kdims[3];
+    int ntap[3][kGrpMaxSA];
+    int tap[3][kGrpMaxSA][kGrpMaxTaps];
+    int off[3][kGrpMaxSA][kGrpMaxTaps];
+    int qw_ext[kGrpMaxS];
+    int n_rowblk;          // ceil(O_d * O_h / kGrpWarps)
+    int taps;              // kD * kH * kW
+};
+
+// slab layout: [tap][ic][COG] (COG >= Cog, zero padded)
+template <typename T, int SW, int COG>
+__global__ void __launch_bounds__(kGrpWarps * 32) grouped_kernel(const __grid_constant__ GroupedParams P) {
+    extern __shared__ float slab[];
+    const T* __restrict__ x = static_cast<const T*>(P.x);
+    const T* __restrict__ w = static_cast<const T*>(P.w);
+    const T* __restrict__ bias = static_cast<const T*>(P.bias);
+    T* __restrict__ y = static_cast<T*>(P.y);
+
+    int64_t blk = blockIdx.x;
+    const int rb = (int)(blk % P.n_rowblk); blk /= P.n_rowblk;
+    const int g = (int)(blk % P.G);
+    const int64_t b = blk / P.G;
+
+    // stage the group's weights: w[g*Cig + ic][oc][tap] -> slab[tap][ic][oc]
+    const int slab_n = P.taps * P.Cig * COG;
+    for (int e = threadIdx.x; e < slab_n; e += blockDim.x) {
+        const int oc = e % COG;
+        const int ic = (e / COG) % P.Cig;
+        const int t = e / (COG * P.Cig);
+        float v = 0.f;
+        if (oc < P.Cog) v = to_f32(w[((int64_t)(g * P.Cig + ic) * P.Cog + oc) * P.taps + t]);
+        slab[e] = v;
+    }
+    __syncthreads();
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int row = rb * kGrpWarps + warp;
+    if (row >= P.O[0] * P.O[1]) return;  // after the only barrier
+    const int od = row / P.O[1], oh = row % P.O[1];
+    const int rd = od % P.S[0], qd = od / P.S[0];
+    const int rh = oh % P.S[1], qh = oh / P.S[1];
+    const int nd_ = P.ntap[0][rd], nh_ = P.ntap[1][rh];
+
+    float bv[COG];
+#pragma unroll
+    for (int oc = 0; oc < COG; ++oc)
+        bv[oc] = (bias != nullptr && oc < P.Cog) ? to_f32(bias[g * P.Cog + oc]) : 0.f;
+
+    const int64_t in_plane = (int64_t)P.I[0] * P.I[1] * P.I[2];
+    const T* xg = x + (b * P.C_in + (int64_t)g * P.Cig) * in_plane;
+    const int64_t out_plane = (int64_t)P.O[0] * P.O[1] * P.O[2];
+    T* yrow = y + (b * P.C_out + (int64_t)g * P.Cog) * out_plane +
+              ((int64_t)od * P.O[1] + oh) * P.O[2];
+
+    const int nq = P.qw_ext[0];  // residue 0 has the most positions
+    for (int q = lane; q - lane < nq; q += 32) {
+        float acc[SW][COG];
+#pragma unroll
+        for (int r = 0; r < SW; ++r)
+#pragma unroll
+            for (int oc = 0; oc < COG; ++oc) acc[r][oc] = 0.f;
+
+#pragma unroll
+        for (int r = 0; r < SW; ++r) {
+            const int nw_ = P.ntap[2][r];
+            if (q >= P.qw_ext[r]) continue;
+            for (int jd = 0; jd < nd_; ++jd) {
+                const int id = qd + P.off[0][rd][jd];
+                if (id < 0 || id >= P.I[0]) continue;
+                for (int jh = 0; jh < nh_; ++jh) {
+                    const int ih = qh + P.off[1][rh][jh];
+                    if (ih < 0 || ih >= P.I[1]) continue;
+                    const T* xr = xg + ((int64_t)id * P.I[1] + ih) * P.I[2];
+                    const int tdh = (P.tap[0][rd][jd] * P.Kdims[1] + P.tap[1][rh][jh]) * P.Kdims[2];
+                    for (int jw = 0; jw < nw_; ++jw) {
+                        const int iw = q + P.off[2][r][jw];
+                        if (iw < 0 || iw >= P.I[2]) continue;
+                        const float* ws = slab + (int64_t)(tdh + P.tap[2][r][jw]) * P.Cig * COG;
+                        const T* xp = xr + iw;
+                        for (int ic = 0; ic < P.Cig; ++ic) {
+                            const float xv = to_f32(xp[(int64_t)ic * in_plane]);
+                            const float* wv = ws + ic * COG;
+#pragma unroll
+                            for (int oc = 0; oc < COG; ++oc) acc[r][oc] = fmaf(xv, wv[oc], acc[r][oc]);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int oc = 0; oc < COG; ++oc) {
+            if (oc >= P.Cog) break;
+#pragma unroll
+            for (int r = 0; r < SW; ++r)
+                if (q < P.qw_ext[r])
+                    yrow[(int64_t)oc * out_plane + r + (int64_t)SW * q] = from_f32<T>(acc[r][oc] + bv[oc]);
+        }
+    }
+}
+
+struct GroupedPlan {
+    AxisPlan ax[3];
+    int cog_pad;
+};
+
+int pad_cog(int cog) {
+    if (cog <= 1) return 1;
+    if (cog <= 2) return 2;
+    if (cog <= 4) return 4;
+    if (cog <= 8) return 8;
+    return 16;
+}
+
+bool make_plan(const Problem& p, GroupedPlan* pl) {
+    if (p.Cog > 16) return false;
+    if (p.S[2] > kGrpMaxS || p.S[0] > kGrpMaxSA || p.S[1] > kGrpMaxSA) return false;
+    for (int a = 0; a < 3; ++a) {
+        plan_axis(p, a, &pl->ax[a]);
+        for (int r = 0; r < p.S[a]; ++r)
+            if (pl->ax[a].ntaps[r] > kGrpMaxTaps) return false;
+    }
+    pl->cog_pad = pad_cog(p.Cog);
+    const size_t slab = (size_t)p.taps() * p.Cig * pl->cog_pad * sizeof(float);
+    if (slab > kGrpMaxSlab) return false;
+    if (p.O[0] * p.O[1] >= (1ll << 30)) return false;
+    return true;
+}
+
+template <typename T, int SW, int COG>
+cudaError_t launch_grouped_t(const GroupedParams& P, int64_t blocks, size_t slab, cudaStream_t stream) {
+    grouped_kernel<T, SW, COG><<<(unsigned)blocks, kGrpWarps * 32, slab, stream>>>(P);
+    return cudaGetLastError();
+}
+
+template <typename T, int SW>
+cudaError_t dispatch_cog(int cog, const GroupedParams& P, int64_t blocks, size_t slab,
+                         cudaStream_t stream) {
+    switch (cog) {
+        case 1: return launch_grouped_t<T, SW, 1>(P, blocks, slab, stream);
+        case 2: return launch_grouped_t<T, SW, 2>(P, blocks, slab, stream);
+        case 4: return launch_grouped_t<T, SW, 4>(P, blocks, slab, stream);
+        case 8: return launch_grouped_t<T, SW, 8>(P, blocks, slab, stream);
+        default: return launch_grouped_t<T, SW, 16>(P, blocks, slab, stream);
+    }
+}
+
+template <typename T>
+cudaError_t dispatch_sw(int sw, int cog, const GroupedParams& P, int64_t blocks, size_t slab,
+                        cudaStream_t stream) {
+    switch (sw) {
+        case 1: return dispatch_cog<T, 1>(cog, P, blocks, slab, stream);
+        case 2: return dispatch_cog<T, 2>(cog, P, blocks, slab, stream);
+        case 3: return dispatch_cog<T, 3>(cog, P, blocks, slab, stream);
+        default: return dispatch_cog<T, 4>(cog, P, blocks, slab, stream);
+    }
+}
+
+}  // namespace
+
+bool grouped_supports(const Problem& p) {
+    GroupedPlan pl;
+    return make_plan(p, &pl);
+}
+
+bool grouped_preferred(const Problem& p) { return p.Cog <= 16; }
+
+cudaError_t launch_grouped(const Problem& p, const void* x, const void* w, const void* bias,
+                           void* y, cudaStream_t stream, Profile* prof) {
+    GroupedPlan pl;
+    if (!make_plan(p, &pl)) return cudaErrorInvalidValue;
+    GroupedParams P;
+    std::memset(&P, 0, sizeof(P));
+    P.x = x;
+    P.w = w;
+    P.bias = bias;
+    P.y = y;
+    P.C_in = (int)p.C_in;
+    P.C_out = (int)p.C_out;
+    P.G = p.G;
+    P.Cig = p.Cig;
+    P.Cog = p.Cog;
+    for (int a = 0; a < 3; ++a) {
+        P.I[a] = (int)p.I[a];
+        P.O[a] = (int)p.O[a];
+        P.S[a] = p.S[a];
+        P.Kdims[a] = (int)p.K[a];
+        for (int r = 0; r < p.S[a]; ++r) {
+            P.ntap[a][r] = pl.ax[a].ntaps[r];
+            for (int j = 0; j < pl.ax[a].ntaps[r]; ++j) {
+                P.tap[a][r][j] = pl.ax[a].tap[r][j];
+                P.off[a][r][j] = pl.ax[a].off[r][j];
+            }
+        }
+    }
+    for (int r = 0; r < p.S[2]; ++r) P.qw_ext[r] = (int)pl.ax[2].q_extent[r];
+    P.taps = (int)p.taps();
+    P.n_rowblk = (int)((p.O[0] * p.O[1] + kGrpWarps - 1) / kGrpWarps);
+    const int64_t blocks = p.B * (int64_t)p.G * P.n_rowblk;
+    if (blocks >= (1ll << 31)) return cudaErrorInvalidConfiguration;
+    const size_t slab = (size_t)P.taps * P.Cig * pl.cog_pad * sizeof(float);
+    prof_begin(prof, stream);
+    cudaError_t e;
+    switch (p.dtype) {
+        case CT_F32: e = dispatch_sw<float>(p.S[2], pl.cog_pad, P, blocks, slab, stream); break;
+        case CT_F16: e = dispatch_sw<__half>(p.S[2], pl.cog_pad, P, blocks, slab, stream); break;
+        default: e = dispatch_sw<__nv_bfloat16>(p.S[2], pl.cog_pad, P, blocks, slab, stream); break;
+    }
+    prof_end(prof, stream);
+    prof_count(prof);
+    return e;
 }
 
 }  // namespace ct

@@ -1,14 +1,286 @@
-// ct_simt.cu -- fp32 stride-phase implicit GEMM on CUDA cores.
+// ct_simt.cu -- fp32 stride-phase implicit GEMM on CUDA cores (FFMA).
+//
+// Same decomposition as the tensor-core route: outputs are split by their
+// residue on every axis, and within one phase each output row
+// (b, od, oh) and W residue rw is a dense GEMM
+//     Y[oc, q] = sum_{(td,th,tw) in T(rd) x T(rh) x T(rw), ic} W'[t][ic][oc] * X[b, ic, id, ih, q + off_w]
+// with id = qd + off_d, ih = qh + off_h -- the stride-phase tiled GEMM the
+// ONNX page lists for 1-D and 2-D (conv-transpose1d-phase-tiled,
+// conv-transpose2d-phase-gemm-tiled) -- computed here in exact fp32 FMA so
+// that fp32 problems keep fp32 accuracy.  Two kernels run:
+//   1. simt_weight_reorder : w [C_in, C_out, taps] -> W' [taps][C_in_pad][N_pad]
+//   2. simt_phase_gemm     : 128 (oc) x 128 (q) tiles, K in steps of 8,
+//      256 threads with 8 x 8 register tiles, both operands double-buffered
+//      in shared memory through cp.async (weights 16 bytes at a time, the
+//      tap-shifted x window 4 bytes at a time since its start is arbitrary),
+//      bias added in fp32 at the end.
+#include <algorithm>
+#include <cstring>
+
 #include "ct_routes.h"
+#include "ct_types.cuh"
 
 namespace ct {
+namespace {
 
-bool simt_supports(const Problem&) { return false; }
-bool simt_preferred(const Problem&) { return false; }
-size_t simt_workspace_bytes(const Problem&) { return 0; }
-cudaError_t launch_simt(const Problem&, const void*, const void*, const void*, void*, void*,
-                        cudaStream_t, Profile*) {
-    return cudaErrorNotSupported;
+constexpr int kBM = 128;  // output channels per tile
+constexpr int kBN = 128;  // q positions per tile
+constexpr int kBK = 8;    // reduction step
+constexpr int kSimtThreads = 256;
+constexpr int kSimtMaxS = 8;
+constexpr int kSimtMaxTaps = 16;
+
+struct SimtParams {
+    const float* x;
+    const float* wp;  // [taps][C_in_pad][N_pad]
+    const float* bias;
+    float* y;
+    int C_in, C_in_pad, C_out, N_pad;
+    int I[3], O[3], S[3], Kdims[3];
+    int ntap[3][kSimtMaxS];
+    int tap[3][kSimtMaxS][kSimtMaxTaps];
+    int off[3][kSimtMaxS][kSimtMaxTaps];
+    int qw_ext[kSimtMaxS];
+    int n_qblk, n_ocblk;
+    int64_t n_blocks;
+};
+
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+
+// 4-byte copy; src_bytes = 0 writes a zero instead of reading.
+__device__ __forceinline__ void cp_async4(float* dst, const float* src, bool valid) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d), "l"(src),
+                 "r"(valid ? 4 : 0)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__global__ void __launch_bounds__(kSimtThreads, 2) simt_phase_gemm(const __grid_constant__ SimtParams P) {
+    __shared__ __align__(16) float As[2][kBK][kBM];
+    __shared__ __align__(16) float Bs[2][kBK][kBN];
+
+    // block -> (oc block, q block, W residue, output row (b, od, oh))
+    int64_t blk = blockIdx.x;
+    const int ocb = (int)(blk % P.n_ocblk); blk /= P.n_ocblk;
+    const int qb = (int)(blk % P.n_qblk); blk /= P.n_qblk;
+    const int rw = (int)(blk % P.S[2]); blk /= P.S[2];
+    const int oh = (int)(blk % P.O[1]); blk /= P.O[1];
+    const int od = (int)(blk % P.O[0]);
+    const int64_t b = blk / P.O[0];
+    const int rd = od % P.S[0], qd = od / P.S[0];
+    const int rh = oh % P.S[1], qh = oh / P.S[1];
+    const int oc0 = ocb * kBM, q0 = qb * kBN;
+    const int qext = P.qw_ext[rw];
+    if (q0 >= qext) return;  // uniform per block
+
+    const int tid = threadIdx.x;
+    const int tx = tid % 16, ty = tid / 16;
+
+    const int nd_ = P.ntap[0][rd], nh_ = P.ntap[1][rh], nw_ = P.ntap[2][rw];
+    const int ntaps = nd_ * nh_ * nw_;
+    const int kchunks = P.C_in_pad / kBK;
+    const int nk = ntaps * kchunks;
+
+    const int64_t in_plane = (int64_t)P.I[0] * P.I[1] * P.I[2];
+    const float* xb = P.x + b * P.C_in * in_plane;
+
+    // loader assignment: A tile 8 x 128 floats = 256 x float4; B tile 8 x 128
+    // floats = 256 threads x 4 floats
+    const int a_k = tid / 32, a_c = (tid % 32) * 4;
+    const int b_k = tid / 32, b_c = (tid % 32) * 4;
+
+    auto load_tile = [&](int kt, int buf) {
+        const int j = kt / kchunks;
+        const int ic0 = (kt % kchunks) * kBK;
+        const int jw = j % nw_;
+        const int jh = (j / nw_) % nh_;
+        const int jd = j / (nw_ * nh_);
+        const int td = P.tap[0][rd][jd], th = P.tap[1][rh][jh], tw = P.tap[2][rw][jw];
+        const int tap = (td * P.Kdims[1] + th) * P.Kdims[2] + tw;
+        // weights: row (tap, ic0 + a_k), channels oc0 + a_c .. +3
+        cp_async16(&As[buf][a_k][a_c],
+                   P.wp + ((int64_t)tap * P.C_in_pad + ic0 + a_k) * P.N_pad + oc0 + a_c);
+        // x window: channel ic0 + b_k, row (id, ih), positions q0 + b_c + i + off_w
+        const int ic = ic0 + b_k;
+        const int id = qd + P.off[0][rd][jd];
+        const int ih = qh + P.off[1][rh][jh];
+        const int iw0 = q0 + b_c + P.off[2][rw][jw];
+        const bool row_ok = ic < P.C_in && id >= 0 && id < P.I[0] && ih >= 0 && ih < P.I[1];
+        const float* xr = xb + (int64_t)ic * in_plane + ((int64_t)id * P.I[1] + ih) * P.I[2];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int iw = iw0 + i;
+            const bool ok = row_ok && iw >= 0 && iw < P.I[2];
+            cp_async4(&Bs[buf][b_k][b_c + i], ok ? xr + iw : P.x, ok);
+        }
+    };
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+    if (nk > 0) {
+        load_tile(0, 0);
+        cp_async_commit();
+        for (int kt = 0; kt < nk; ++kt) {
+            const int buf = kt & 1;
+            if (kt + 1 < nk) {
+                load_tile(kt + 1, buf ^ 1);
+                cp_async_commit();
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
+            }
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < kBK; ++k) {
+                const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][k][ty * 4]);
+                const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][k][ty * 4 + 64]);
+                const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][k][tx * 4]);
+                const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][k][tx * 4 + 64]);
+                const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
+            }
+            __syncthreads();
+        }
+    }
+
+    // epilogue: y[b, oc, od, oh, ow = rw + s_w * q] = acc + bias[oc]
+    const int64_t plane = (int64_t)P.O[0] * P.O[1] * P.O[2];
+    const int64_t row_off = ((int64_t)od * P.O[1] + oh) * P.O[2];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int oc = oc0 + ty * 4 + (i & 3) + (i >> 2) * 64;
+        if (oc >= P.C_out) continue;
+        const float bv = P.bias ? P.bias[oc] : 0.f;
+        float* yr = P.y + (b * P.C_out + oc) * plane + row_off;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int q = q0 + tx * 4 + (j & 3) + (j >> 2) * 64;
+            if (q < qext) yr[rw + (int64_t)P.S[2] * q] = acc[i][j] + bv;
+        }
+    }
+}
+
+// W'[t][c][n] = w[c][n][t] for c < C_in, n < C_out; 0 in the padding.
+__global__ void simt_weight_reorder(const float* __restrict__ w, float* __restrict__ wp, int C_in,
+                                    int C_out, int taps, int C_in_pad, int N_pad) {
+    const int64_t total = (int64_t)taps * C_in_pad * N_pad;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int n = (int)(e % N_pad);
+        const int c = (int)((e / N_pad) % C_in_pad);
+        const int t = (int)(e / ((int64_t)N_pad * C_in_pad));
+        wp[e] = (c < C_in && n < C_out) ? w[((int64_t)c * C_out + n) * taps + t] : 0.f;
+    }
+}
+
+struct SimtPlan {
+    int C_in_pad, N_pad;
+    AxisPlan ax[3];
+};
+
+bool make_plan(const Problem& p, SimtPlan* pl) {
+    if (p.dtype != CT_F32 || p.G != 1) return false;
+    for (int a = 0; a < 3; ++a) {
+        if (p.S[a] > kSimtMaxS) return false;
+        plan_axis(p, a, &pl->ax[a]);
+        for (int r = 0; r < p.S[a]; ++r)
+            if (pl->ax[a].ntaps[r] > kSimtMaxTaps) return false;
+    }
+    pl->C_in_pad = (int)((p.C_in + kBK - 1) / kBK * kBK);
+    pl->N_pad = (int)((p.C_out + kBM - 1) / kBM * kBM);
+    return true;
+}
+
+}  // namespace
+
+bool simt_supports(const Problem& p) {
+    SimtPlan pl;
+    return make_plan(p, &pl);
+}
+
+bool simt_preferred(const Problem& p) {
+    // worth the tile machinery once the reduction and the channel count fill a tile
+    return p.C_in >= 32 && p.C_out >= 32;
+}
+
+size_t simt_workspace_bytes(const Problem& p) {
+    SimtPlan pl;
+    if (!make_plan(p, &pl)) return 0;
+    return ((size_t)p.taps() * pl.C_in_pad * pl.N_pad * 4 + 255) / 256 * 256;
+}
+
+cudaError_t launch_simt(const Problem& p, const void* x, const void* w, const void* bias, void* y,
+                        void* workspace, cudaStream_t stream, Profile* prof) {
+    SimtPlan pl;
+    if (!make_plan(p, &pl)) return cudaErrorInvalidValue;
+    DeviceInfo dev;
+    cudaError_t e = device_info(&dev);
+    if (e != cudaSuccess) return e;
+    float* wp = static_cast<float*>(workspace);
+    {
+        const int64_t tot = p.taps() * pl.C_in_pad * pl.N_pad;
+        const int blocks = (int)std::min<int64_t>((tot + 255) / 256, (int64_t)dev.sm_count * 8);
+        simt_weight_reorder<<<blocks, 256, 0, stream>>>(static_cast<const float*>(w), wp,
+                                                        (int)p.C_in, (int)p.C_out, (int)p.taps(),
+                                                        pl.C_in_pad, pl.N_pad);
+        prof_count(prof);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    SimtParams P;
+    std::memset(&P, 0, sizeof(P));
+    P.x = static_cast<const float*>(x);
+    P.wp = wp;
+    P.bias = static_cast<const float*>(bias);
+    P.y = static_cast<float*>(y);
+    P.C_in = (int)p.C_in;
+    P.C_in_pad = pl.C_in_pad;
+    P.C_out = (int)p.C_out;
+    P.N_pad = pl.N_pad;
+    for (int a = 0; a < 3; ++a) {
+        P.I[a] = (int)p.I[a];
+        P.O[a] = (int)p.O[a];
+        P.S[a] = p.S[a];
+        P.Kdims[a] = (int)p.K[a];
+        for (int r = 0; r < p.S[a]; ++r) {
+            P.ntap[a][r] = pl.ax[a].ntaps[r];
+            for (int j = 0; j < pl.ax[a].ntaps[r]; ++j) {
+                P.tap[a][r][j] = pl.ax[a].tap[r][j];
+                P.off[a][r][j] = pl.ax[a].off[r][j];
+            }
+        }
+    }
+    for (int r = 0; r < p.S[2]; ++r) P.qw_ext[r] = (int)pl.ax[2].q_extent[r];
+    P.n_qblk = (int)((pl.ax[2].q_extent[0] + kBN - 1) / kBN);
+    P.n_ocblk = pl.N_pad / kBM;
+    const int64_t blocks =
+        p.B * p.O[0] * p.O[1] * (int64_t)p.S[2] * P.n_qblk * (int64_t)P.n_ocblk;
+    if (blocks >= (1ll << 31)) return cudaErrorInvalidConfiguration;
+    P.n_blocks = blocks;
+    prof_begin(prof, stream);
+    simt_phase_gemm<<<(unsigned)blocks, kSimtThreads, 0, stream>>>(P);
+    prof_end(prof, stream);
+    prof_count(prof);
+    return cudaGetLastError();
 }
 
 }  // namespace ct
