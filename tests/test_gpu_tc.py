@@ -99,3 +99,23 @@ def test_tc_matches_gather_bits_closely():
     torch.cuda.synchronize()
     bound = torch.abs(yg) * 2.0 ** -7 + 1e-5 * float(torch.abs(yg).max())
     assert bool((torch.abs(yt - yg) <= bound).all())
+
+
+def test_tc_route_with_unaligned_x_and_odd_spatial_size():
+    """x starting 2 bytes past a 16-byte boundary and D*H*W not a multiple of
+    8 take the layout pass's element-wise path; results must not change."""
+    p = synth.problem("tc_unaligned", 2, 64, 32, (7, 9), 3, stride=2, pad=1, dtype="bf16",
+                      seed=217)
+    x, w, b = synth.make_inputs(p)
+    ref = oracle.conv_transpose(x, w, b, **p.attrs())
+    flat = torch.empty(x.numel() + 8, dtype=x.dtype, device="cuda")
+    xs = flat[1:1 + x.numel()].view(x.shape)
+    xs.copy_(x.cuda())
+    assert xs.data_ptr() % 16 != 0
+    O = ct.ct_conv_transpose_out_shape(p.spatial, p.k, p.stride, p.pad_lo, p.pad_hi,
+                                       p.dilation, p.output_padding)
+    y = torch.empty((p.B, p.C_out) + O, dtype=p.torch_dtype, device="cuda")
+    ct.ct_conv_transpose_nd(xs, w.cuda(), b.cuda(), y, None, p.stride, p.pad_lo, p.pad_hi,
+                            p.dilation, p.output_padding, p.groups, ct.CT_ROUTE_TC_GEMM)
+    torch.cuda.synchronize()
+    assert_close(p, y, ref, "tc route, unaligned x")

@@ -514,28 +514,55 @@ __global__ void tc_weight_reorder(const T* __restrict__ w, T* __restrict__ wp, i
     }
 }
 
-// X'[b][s][c] = x[b][c][s] for c < C, 0 for C <= c < C_pad.  64 x 64 tiles
-// through shared memory: reads are coalesced along s, writes along c.
+// X'[b][s][c] = x[b][c][s] for c < C, 0 for C <= c < C_pad.  One block moves
+// a 64 (c) x 64 (s) tile through shared memory:
+// 16-byte loads along s (when S % 8 == 0 and x is 16-byte aligned; 2-byte
+// loads otherwise) and 16-byte stores along c; the tile is stored with
+// its 8-element column chunks XOR-swizzled by row so that both the scattered
+// 2-byte writes and the 16-byte row reads avoid bank conflicts.
 template <typename T>
 __global__ void __launch_bounds__(256) tc_channels_last(const T* __restrict__ x, T* __restrict__ xc,
-                                                        int C, int C_pad, int64_t S) {
-    __shared__ uint16_t tile[64][66];
+                                                        int C, int C_pad, int64_t S, bool vec) {
+    __shared__ __align__(16) uint16_t tile[64][64];
     const int64_t s0 = (int64_t)blockIdx.x * 64;
     const int c0 = blockIdx.y * 64;
     const int64_t b = blockIdx.z;
-    const int tx = threadIdx.x % 64, ty = threadIdx.x / 64;
     const uint16_t* xs = reinterpret_cast<const uint16_t*>(x);
     uint16_t* xd = reinterpret_cast<uint16_t*>(xc);
-    for (int c = ty; c < 64; c += 4) {
-        uint16_t v = 0;
-        const int64_t s = s0 + tx;
-        if (c0 + c < C && s < S) v = xs[(b * C + c0 + c) * S + s];
-        tile[c][tx] = v;
+    const int t = threadIdx.x;
+    // load: thread -> (c = t/8 + 32*i, s chunk = t%8)
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int c = t / 8 + 32 * i;
+        const int sv = t % 8;
+        uint16_t v[8];
+        const int64_t s = s0 + sv * 8;
+        if (c0 + c < C && vec && s + 8 <= S) {
+            const uint4 u = *reinterpret_cast<const uint4*>(xs + (b * C + c0 + c) * S + s);
+            const uint16_t* h = reinterpret_cast<const uint16_t*>(&u);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = h[j];
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[j] = (c0 + c < C && s + j < S) ? xs[(b * C + c0 + c) * S + s + j] : 0;
+        }
+        // element (s_local = sv*8 + j, c) -> row s_local, chunk (c/8) ^ (j ^ sv)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            tile[sv * 8 + j][(((c >> 3) ^ j ^ sv) << 3) | (c & 7)] = v[j];
     }
     __syncthreads();
-    for (int s = ty; s < 64; s += 4) {
-        const int64_t ss = s0 + s;
-        if (ss < S) xd[(b * S + ss) * C_pad + c0 + tx] = tile[tx][s];
+    // store: thread -> (s = t/8 + 32*i, c chunk = t%8)
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int sl = t / 8 + 32 * i;
+        const int cv = t % 8;
+        const int64_t s = s0 + sl;
+        if (s >= S) continue;
+        const int key = (sl & 7) ^ (sl >> 3);
+        const uint4 u = *reinterpret_cast<const uint4*>(&tile[sl][(cv ^ key) << 3]);
+        *reinterpret_cast<uint4*>(xd + (b * S + s) * C_pad + c0 + cv * 8) = u;
     }
 }
 
@@ -732,8 +759,10 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
         const int64_t S = p.in_spatial();
         dim3 grid((unsigned)((S + 63) / 64), (unsigned)(pl.C_pad / 64), (unsigned)p.B);
         if (grid.y > 65535 || grid.z > 65535) return cudaErrorInvalidConfiguration;
+        // 16-byte loads need S % 8 == 0 and a 16-byte aligned x
+        const bool vec = (S % 8) == 0 && ((uintptr_t)x % 16) == 0;
         tc_channels_last<T><<<grid, 256, 0, stream>>>(static_cast<const T*>(x), xc, (int)p.C_in,
-                                                      pl.C_pad, S);
+                                                      pl.C_pad, S, vec);
         prof_count(prof);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
