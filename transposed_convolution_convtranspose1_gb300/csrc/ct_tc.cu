@@ -4,34 +4,42 @@
 // every axis (stride phases).  Within a phase every output o = r + s*q
 // receives the same set of taps T_r, each reading input i = q + off(r, t), so
 // the phase is a dense GEMM
-//     Y_r[b, q, oc] = sum_{t in T_r, ic} X[b, q + off(r,t), ic] * W[t][oc][ic]
+//     Y_r[b, oc, q] = sum_{t in T_r, ic} W[t][oc][ic] * X[b, q + off(r,t), ic]
 // over C_in x |T_r| -- the ONNX page's implicit-gather GEMM with tap-reversed
 // weights (ai.onnx.ConvTranspose, variant ncdhw3d_implicit_sgmat: no column
 // matrix, no scatter pass, reduction over the full in-channel-by-tap depth),
 // generalised from stride 1 to every stride phase.  Three kernels run:
 //   1. tc_weight_reorder : w [C_in, C_out, taps] -> W' [taps][N_pad][C_pad]
-//                          (K-major B operand, zero padded; taps indexed in the
+//                          (K-major A operand, zero padded; taps indexed in the
 //                          pages' unflipped order, visited per phase in
 //                          reversed order, i.e. increasing input offset)
 //   2. tc_channels_last  : x [B, C, D*H*W] -> X' [B, D, H, W, C_pad]
-//                          (K-major A operand; TMA boxes then shift along the
+//                          (K-major B operand; TMA boxes then shift along the
 //                          spatial axes only, so every box starts on a
 //                          128-byte boundary of the channel axis)
-//   3. tc_phase_gemm     : persistent, warp-specialised:
-//        warp 0      TMA producer: per k-block one 5-D box of X' shifted by
-//                    the tap's input offset (out-of-range rows zero-filled by
-//                    TMA) and one box of W', into a ring of SW128 stages
-//        warp 1      TMEM allocator and single-thread tcgen05.mma issuer,
-//                    M = 128 output positions, N = output-channel tile,
+//   3. tc_phase_gemm     : persistent, warp-specialised, one CTA per SM:
+//        warp 0      TMA producer: per k-block (one tap, 64 input channels)
+//                    a box of W' (128 output channels) and a 5-D box of X'
+//                    (NP output positions, shifted by the tap's input
+//                    offsets; rows outside the input are zero-filled by TMA)
+//                    into a ring of 128-byte-swizzled stages
+//        warp 1      TMEM allocator and single-thread tcgen05.mma issuer:
+//                    D[oc, position] += W'[oc, k] X'[position, k], M = 128
+//                    output channels, N = NP positions (256 for strides 1-2),
 //                    K = 16 per instruction, fp32 accumulators in TMEM
-//        warps 2..5  epilogue: tcgen05.ld, + bias in fp32, one RNE rounding,
-//                    stores interleaving the W phases of a tile so that a warp
-//                    writes whole output rows
-//      A tile holds every W phase of its positions (one accumulator each);
-//      accumulators are double-buffered so the epilogue of one tile overlaps
-//      the MMAs of the next.  Every mbarrier wait is bounded: on time-out the
-//      kernel records a code in g_device_error, stops issuing work, drains
-//      its outstanding copies and MMAs (bounded too), frees TMEM and returns.
+//        warps 2..5  epilogue: tcgen05.ld of each W phase's accumulator
+//                    (one lane per output channel), + bias in fp32, one RNE
+//                    rounding, the W phases of a position interleaved in
+//                    registers so that each lane writes runs of consecutive
+//                    outputs of its channel's row with 16-byte stores.
+//      Why N = positions: one thread issues every MMA and each barrier wait
+//      costs it a few hundred cycles, so an MMA must carry enough work
+//      (M = 128, N = 256: 128 tensor cycles) for four of them to cover a wait.
+//      Accumulators are double-buffered when they fit (stride 1), so the
+//      epilogue of one tile overlaps the MMAs of the next.  Every mbarrier
+//      wait is bounded: on time-out the kernel records a code in
+//      g_device_error, stops issuing work, drains its outstanding copies and
+//      MMAs (bounded too), frees TMEM and returns.
 #include <algorithm>
 #include <cstring>
 #include <mutex>
@@ -49,10 +57,11 @@ __device__ unsigned int g_device_error = 0;
 
 namespace {
 
-constexpr int kTcMaxS = 8;        // stride per axis on this route
+constexpr int kTcMaxS = 8;        // D / H stride on this route
+constexpr int kTcMaxSW = 4;       // W stride on this route (W phases per tile)
 constexpr int kTcMaxTaps = 8;     // taps per axis and phase on this route
 constexpr int kTcMaxClasses = 32; // (D residue, H residue) classes
-constexpr int kBlockM = 128;      // output positions per tile (TMEM lanes)
+constexpr int kBlockM = 128;      // output channels per tile (TMEM lanes)
 constexpr int kBlockK = 64;       // channels per k-block (one 128-byte row)
 constexpr int kThreads = 192;     // 6 warps
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait before giving up
@@ -71,17 +80,17 @@ struct TcClass {
 };
 
 struct TcParams {
-    CUtensorMap tmap_a;   // X' [B, D, H, W, C_pad] as 5-D (C_pad, W, H, D, B)
-    CUtensorMap tmap_b;   // W' [taps][N_pad][C_pad] as 3-D (C_pad, N_pad, taps)
+    CUtensorMap tmap_w;   // W' [taps][N_pad][C_pad] as 3-D (C_pad, N_pad, taps)
+    CUtensorMap tmap_x;   // X' [B, D, H, W, C_pad] as 5-D (C_pad, W, H, D, B)
     const void* bias;
     void* y;
-    int C_out, n_kblk, n_tile, n_oc_tiles;
+    int C_out, n_kblk, n_oc_tiles;
     int O[3];
     int S[3];
     int Kdims[3];         // kD, kH, kW (for the flat tap index)
-    int WC, MR;           // tile = MR rows of WC positions along W
-    int sw;               // W stride = number of W phases per tile
-    int qw_ext[kTcMaxS];  // q extent of each W residue
+    int NP;               // output positions per tile (MMA N)
+    int WC, MR;           // tile positions = MR rows of WC positions along W
+    int qw_ext[kTcMaxSW]; // q extent of each W residue
     int ntap[3][kTcMaxS];
     int tap[3][kTcMaxS][kTcMaxTaps];
     int off[3][kTcMaxS][kTcMaxTaps];
@@ -91,7 +100,9 @@ struct TcParams {
     uint32_t stage_bytes, a_bytes;
     uint32_t idesc;
     uint32_t tmem_cols;
-    int acc_stride;       // TMEM columns per accumulator buffer (sw * n_tile)
+    int acc_stride;       // TMEM columns per accumulator buffer (sw * NP)
+    int n_buf;            // accumulator buffers (1 or 2)
+    int vec_store;        // 16-byte output stores allowed (O_w % 8 == 0, y aligned)
 };
 
 // ---------------------------------------------------------------------------
@@ -231,6 +242,24 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -260,28 +289,31 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& P, int t) {
     T.b = local / C.n_qd;
     T.qh0 = qh_b * P.MR;
     T.qw0 = qw_b * P.WC;
-    T.oc0 = oc_t * P.n_tile;
+    T.oc0 = oc_t * kBlockM;
     return T;
 }
 
+template <int SW>
 __device__ __forceinline__ int phase_taps(const TcParams& P, const Tile& T, int rw) {
     return P.ntap[0][T.rd] * P.ntap[1][T.rh] * P.ntap[2][rw];
 }
 
+template <int SW>
 __device__ __forceinline__ bool tile_has_work(const TcParams& P, const Tile& T) {
-    for (int rw = 0; rw < P.sw; ++rw)
-        if (phase_taps(P, T, rw) > 0) return true;
+#pragma unroll
+    for (int rw = 0; rw < SW; ++rw)
+        if (phase_taps<SW>(P, T, rw) > 0) return true;
     return false;
 }
 
 // ---------------------------------------------------------------------------
-// the GEMM kernel
+// the GEMM kernel; SW = W stride (W phases per tile)
 // ---------------------------------------------------------------------------
 
-template <typename T>
+template <typename T, int SW>
 __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_constant__ TcParams P) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ uint64_t full_bar[16], empty_bar[16], tfull_bar[2], tempty_bar[2], drain_bar;
+    __shared__ uint64_t full_bar[8], empty_bar[8], tfull_bar[2], tempty_bar[2], drain_bar;
     __shared__ uint32_t tmem_base_slot;
     __shared__ volatile int abort_flag;
 
@@ -305,9 +337,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (warp == 0 && lane == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_a))
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_w))
                      : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_b))
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_x))
                      : "memory");
     }
     if (warp == 1) {
@@ -325,11 +357,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         // The whole warp walks the schedule; lane 0 issues the copies.
-        uint32_t kiter = 0;
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
             const Tile tl = decode_tile(P, t);
-            for (int rw = 0; rw < P.sw && ok; ++rw) {
+            for (int rw = 0; rw < SW && ok; ++rw) {
                 const int nd_ = P.ntap[0][tl.rd], nh_ = P.ntap[1][tl.rh], nw_ = P.ntap[2][rw];
                 for (int jd = 0; jd < nd_ && ok; ++jd)
                     for (int jh = 0; jh < nh_ && ok; ++jh)
@@ -341,138 +375,161 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                             const int ih = tl.qh0 + P.off[1][tl.rh][jh];
                             const int iw = tl.qw0 + P.off[2][rw][jw];
                             for (int kb = 0; kb < P.n_kblk; ++kb) {
-                                const int s = kiter % P.stages;
-                                const uint32_t par = ((kiter / P.stages) & 1) ^ 1;
                                 ok = __all_sync(0xffffffffu,
-                                                mbar_wait(smem_u32(&empty_bar[s]), par,
+                                                mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1,
                                                           kErrProducer, &abort_flag));
                                 if (!ok) break;
                                 if (lane == 0) {
-                                    const uint32_t fb = smem_u32(&full_bar[s]);
-                                    const uint32_t sa = ring + s * P.stage_bytes;
+                                    const uint32_t fb = smem_u32(&full_bar[stage]);
+                                    const uint32_t sa = ring + stage * P.stage_bytes;
                                     mbar_expect_tx(fb, P.stage_bytes);
-                                    tma_load_5d(sa, &P.tmap_a, fb, kb * kBlockK, iw, ih, id, tl.b);
-                                    tma_load_3d(sa + P.a_bytes, &P.tmap_b, fb, kb * kBlockK, tl.oc0,
-                                                tap);
+                                    tma_load_3d(sa, &P.tmap_w, fb, kb * kBlockK, tl.oc0, tap);
+                                    tma_load_5d(sa + P.a_bytes, &P.tmap_x, fb, kb * kBlockK, iw, ih,
+                                                id, tl.b);
                                 }
                                 __syncwarp();
-                                ++kiter;
+                                ++issued;
+                                if (++stage == P.stages) {
+                                    stage = 0;
+                                    phase ^= 1;
+                                }
                             }
                         }
             }
         }
         if (!ok && lane == 0) {
             // every copy issued so far must land before the CTA exits
-            const uint32_t first = kiter > (uint32_t)P.stages ? kiter - P.stages : 0;
-            for (uint32_t k = first; k < kiter; ++k)
+            const uint32_t first = issued > (uint32_t)P.stages ? issued - P.stages : 0;
+            for (uint32_t k = first; k < issued; ++k)
                 mbar_drain(smem_u32(&full_bar[k % P.stages]), (k / P.stages) & 1);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
-        // The whole warp walks the schedule; lane 0 issues MMAs and commits.
-        uint32_t kiter = 0, acc_iter = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
-            const Tile tl = decode_tile(P, t);
-            if (!tile_has_work(P, tl)) continue;
-            const int buf = acc_iter & 1;
-            const uint32_t tpar = ((acc_iter >> 1) & 1) ^ 1;
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(smem_u32(&tempty_bar[buf]), tpar, kErrMma, &abort_flag));
-            if (!ok) break;
-            tc_fence_after();
-            for (int rw = 0; rw < P.sw && ok; ++rw) {
-                const int nk = phase_taps(P, tl, rw) * P.n_kblk;
-                const uint32_t d = tmem_base + buf * P.acc_stride + rw * P.n_tile;
-                for (int j = 0; j < nk; ++j) {
-                    const int s = kiter % P.stages;
-                    const uint32_t par = (kiter / P.stages) & 1;
-                    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[s]), par, kErrMma,
-                                                           &abort_flag));
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t sa = ring + s * P.stage_bytes;
+        // Lane 0 waits and issues; the other lanes wait at the final barrier.
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, acc_iter = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+                const Tile tl = decode_tile(P, t);
+                if (!tile_has_work<SW>(P, tl)) continue;
+                const int buf = P.n_buf == 2 ? (int)(acc_iter & 1) : 0;
+                const uint32_t tpar = (P.n_buf == 2 ? (acc_iter >> 1) : acc_iter) & 1;
+                if (!mbar_wait(smem_u32(&tempty_bar[buf]), tpar ^ 1, kErrMma, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int rw = 0; rw < SW && ok; ++rw) {
+                    const int nk = phase_taps<SW>(P, tl, rw) * P.n_kblk;
+                    const uint32_t d = tmem_base + buf * P.acc_stride + rw * P.NP;
+                    for (int j = 0; j < nk; ++j) {
+                        if (!mbar_wait(smem_u32(&full_bar[stage]), phase, kErrMma, &abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sa = ring + stage * P.stage_bytes;
                         const uint64_t ad = smem_desc_sw128(sa);
                         const uint64_t bd = smem_desc_sw128(sa + P.a_bytes);
 #pragma unroll
                         for (int k = 0; k < kBlockK / 16; ++k) {
                             // advance along K by 16 elements = 32 bytes (encoded >> 4: 2)
-                            mma_f16(d, ad + 2 * k, bd + 2 * k, P.idesc,
-                                    (j > 0 || k > 0) ? 1u : 0u);
+                            mma_f16(d, ad + 2 * k, bd + 2 * k, P.idesc, (j > 0 || k > 0) ? 1u : 0u);
                         }
-                        mma_commit(smem_u32(&empty_bar[s]));
+                        mma_commit(smem_u32(&empty_bar[stage]));
+                        if (++stage == P.stages) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
                     }
-                    __syncwarp();
-                    ++kiter;
                 }
+                if (!ok) break;
+                mma_commit(smem_u32(&tfull_bar[buf]));
+                ++acc_iter;
             }
-            if (!ok) break;
-            if (lane == 0) mma_commit(smem_u32(&tfull_bar[buf]));
-            __syncwarp();
-            ++acc_iter;
-        }
-        // no MMA may be in flight when TMEM is released
-        if (lane == 0) {
+            // no MMA may be in flight when TMEM is released
             mma_commit(smem_u32(&drain_bar));
             mbar_drain(smem_u32(&drain_bar), 0);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;             // TMEM lane quarter this warp may access
-        const int m = q * 32 + lane;        // tile row = output position
-        const int row = m / P.WC, col = m % P.WC;
+        // Warp q (= warp % 4, the TMEM lane quarter it may read) owns output
+        // channels oc0 + 32q .. +31, one per lane.  Per chunk of CQ positions
+        // of one output row, each lane loads its channel's accumulators of all
+        // SW W phases, interleaves them (output s_w*q + rw), adds the bias,
+        // rounds once and writes its SW*CQ consecutive outputs with 16-byte
+        // stores.
+        constexpr int CQ = SW <= 2 ? 32 : 16;   // positions per chunk
+        constexpr int kPieces = SW * CQ / 8;    // 16-byte pieces per lane and chunk
+        const int q = warp & 3;
         const T* __restrict__ bias = static_cast<const T*>(P.bias);
         T* __restrict__ y = static_cast<T*>(P.y);
-        const int64_t chan_rows = (int64_t)P.O[0] * P.O[1];  // output rows per channel
         uint32_t acc_iter = 0;
         for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x) {
             const Tile Tl = decode_tile(P, t);
             const TcClass& C = P.cls[Tl.cls];
-            const bool work = tile_has_work(P, Tl);
-            const int buf = acc_iter & 1;
+            const bool work = tile_has_work<SW>(P, Tl);
+            const int buf = P.n_buf == 2 ? (int)(acc_iter & 1) : 0;
             if (work) {
+                const uint32_t tpar = (P.n_buf == 2 ? (acc_iter >> 1) : acc_iter) & 1;
                 const bool ok = __all_sync(
-                    0xffffffffu, mbar_wait(smem_u32(&tfull_bar[buf]), (acc_iter >> 1) & 1,
-                                           kErrEpilogue, &abort_flag));
+                    0xffffffffu,
+                    mbar_wait(smem_u32(&tfull_bar[buf]), tpar, kErrEpilogue, &abort_flag));
                 if (!ok) break;
                 tc_fence_after();
             }
-            const int qh = Tl.qh0 + row, qw = Tl.qw0 + col;
-            const bool pos_ok = (Tl.qd < C.qd_ext) && (qh < C.qh_ext);
+            const int oc = Tl.oc0 + q * 32 + lane;
+            const bool oc_ok = oc < P.C_out;
+            const float bv = (bias != nullptr && oc_ok) ? to_f32(bias[oc]) : 0.f;
             const int od = Tl.rd + P.S[0] * Tl.qd;
-            const int oh = Tl.rh + P.S[1] * qh;
-            // index of output row (b, oc = 0, od, oh)
-            const int64_t row0 = ((int64_t)Tl.b * P.C_out * P.O[0] + od) * P.O[1] + oh;
-            for (int j0 = 0; j0 < P.n_tile; j0 += 16) {
-                float bv[16];
+            const bool d_ok = Tl.qd < C.qd_ext;
+            const int64_t chan_base = ((int64_t)Tl.b * P.C_out + oc) * P.O[0] + od;
+            for (int p0 = 0; p0 < P.NP; p0 += CQ) {
+                const int row = p0 / P.WC;
+                const int qh = Tl.qh0 + row;
+                const int qwb = Tl.qw0 + (p0 % P.WC);
+                // warp-uniform: the chunk's positions are the same for every lane
+                if (!d_ok || qh >= C.qh_ext || qwb >= P.qw_ext[0]) continue;
+                const int oh = Tl.rh + P.S[1] * qh;
+                float v[SW][CQ];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int oc = Tl.oc0 + j0 + i;
-                    bv[i] = (bias != nullptr && oc < P.C_out) ? to_f32(bias[oc]) : 0.f;
-                }
-                for (int rw = 0; rw < P.sw; ++rw) {
-                    float v[16];
-                    if (work && phase_taps(P, Tl, rw) > 0) {
-                        tmem_ld16(tmem_base + ((uint32_t)(q * 32) << 16) +
-                                      (uint32_t)(buf * P.acc_stride + rw * P.n_tile + j0),
-                                  v);
-                        tmem_ld_wait();
+                for (int rw = 0; rw < SW; ++rw) {
+                    if (work && phase_taps<SW>(P, Tl, rw) > 0) {
+                        const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                            (uint32_t)(buf * P.acc_stride + rw * P.NP + p0);
+                        if constexpr (CQ == 32) tmem_ld32(ta, v[rw]);
+                        else tmem_ld16(ta, v[rw]);
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                        for (int i = 0; i < CQ; ++i) v[rw][i] = 0.f;
                     }
-                    const int ow = rw + P.sw * qw;
-                    if (pos_ok && qw < P.qw_ext[rw]) {
+                }
+                tmem_ld_wait();
+                if (!oc_ok) continue;
+                const int ow0 = SW * qwb;
+                T* dst = y + (chan_base * P.O[1] + oh) * (int64_t)P.O[2] + ow0;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int oc = Tl.oc0 + j0 + i;
-                            if (oc < P.C_out)
-                                y[(row0 + (int64_t)oc * chan_rows) * P.O[2] + ow] =
-                                    from_f32<T>(v[i] + bv[i]);
-                        }
+                for (int c = 0; c < kPieces; ++c) {
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const int j0 = c * 8 + 2 * h, j1 = j0 + 1;  // output j = qi*SW + rw
+                        const T lo = from_f32<T>(v[j0 % SW][j0 / SW] + bv);
+                        const T hi = from_f32<T>(v[j1 % SW][j1 / SW] + bv);
+                        wv[h] = (uint32_t)(*reinterpret_cast<const uint16_t*>(&lo)) |
+                                ((uint32_t)(*reinterpret_cast<const uint16_t*>(&hi)) << 16);
+                    }
+                    const int ow = ow0 + c * 8;
+                    if (P.vec_store && ow + 8 <= P.O[2]) {
+                        *reinterpret_cast<uint4*>(dst + c * 8) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    } else {
+                        uint16_t* d16 = reinterpret_cast<uint16_t*>(dst + c * 8);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            if (ow + i < P.O[2]) d16[i] = (uint16_t)(wv[i >> 1] >> (16 * (i & 1)));
                     }
                 }
             }
@@ -571,41 +628,44 @@ __global__ void __launch_bounds__(256) tc_channels_last(const T* __restrict__ x,
 // ---------------------------------------------------------------------------
 
 struct TcPlan {
-    int C_pad, N_pad, n_tile, n_oc_tiles, sw, WC, MR, stages;
-    size_t x_bytes, w_bytes;
+    int C_pad, N_pad, n_oc_tiles, sw, NP, WC, MR, stages, n_buf;
+    size_t x_bytes, w_bytes, epi_bytes, stage_bytes;
     AxisPlan ax[3];
 };
+
+constexpr size_t kSmemLimit = 232448;  // opt-in shared memory per block (227 KiB)
 
 bool make_plan(const Problem& p, TcPlan* pl) {
     if (p.dtype != CT_BF16 && p.dtype != CT_F16) return false;
     if (p.G != 1) return false;
+    if (p.S[0] > kTcMaxS || p.S[1] > kTcMaxS || p.S[2] > kTcMaxSW) return false;
     for (int a = 0; a < 3; ++a) {
-        if (p.S[a] > kTcMaxS) return false;
         plan_axis(p, a, &pl->ax[a]);
         for (int r = 0; r < p.S[a]; ++r)
             if (pl->ax[a].ntaps[r] > kTcMaxTaps) return false;
     }
     if (p.S[0] * p.S[1] > kTcMaxClasses) return false;
     pl->sw = p.S[2];
-    int nt = (int)((256 / pl->sw) / 16) * 16;  // two accumulator buffers in 512 columns
-    if (nt < 16) return false;
-    const int cout16 = (int)((p.C_out + 15) / 16 * 16);
-    pl->n_tile = std::min(std::min(nt, 256), cout16);
-    pl->n_oc_tiles = (int)((p.C_out + pl->n_tile - 1) / pl->n_tile);
-    pl->N_pad = pl->n_oc_tiles * pl->n_tile;
+    pl->NP = pl->sw <= 2 ? 256 : 128;
+    const int acc_stride = pl->sw * pl->NP;
+    pl->n_buf = 2 * acc_stride <= 512 ? 2 : 1;
+    pl->N_pad = (int)((p.C_out + kBlockM - 1) / kBlockM * kBlockM);
+    pl->n_oc_tiles = pl->N_pad / kBlockM;
     pl->C_pad = (int)((p.C_in + kBlockK - 1) / kBlockK * kBlockK);
     const int64_t qw0 = pl->ax[2].q_extent[0];
-    int wc = 8;
-    while (wc < qw0 && wc < 128) wc *= 2;
+    int wc = 32;  // an epilogue chunk (up to 32 positions) stays within one row
+    while (wc < qw0 && wc < pl->NP) wc *= 2;
     pl->WC = wc;
-    pl->MR = kBlockM / wc;
-    const size_t stage = (size_t)kBlockM * 128 + (size_t)pl->n_tile * 128;
-    pl->stages = (int)std::min<size_t>(8, (227 * 1024 - 2048) / stage);
+    pl->MR = pl->NP / wc;
+    pl->stage_bytes = (size_t)kBlockM * 128 + (size_t)pl->NP * 128;
+    pl->epi_bytes = 0;
+    const size_t room = kSmemLimit - 1024 - pl->epi_bytes - 512;
+    pl->stages = (int)std::min<size_t>(8, room / pl->stage_bytes);
     if (pl->stages < 2) return false;
     pl->x_bytes = (size_t)p.B * p.in_spatial() * pl->C_pad * 2;
     pl->w_bytes = (size_t)p.taps() * pl->N_pad * pl->C_pad * 2;
-    // TMA limits: every global extent < 2^32, strides < 2^40
-    if (p.in_spatial() * (int64_t)pl->C_pad * 2 * p.B >= (1ll << 40)) return false;
+    // TMA limits: strides < 2^40, extents < 2^32
+    if ((double)p.in_spatial() * pl->C_pad * 2 * p.B >= 1e12) return false;
     return true;
 }
 
@@ -623,6 +683,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
     });
     return fn;
+}
+
+template <typename T, int SW>
+cudaError_t launch_gemm(const TcParams& P, int grid, size_t smem, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(tc_phase_gemm<T, SW>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    tc_phase_gemm<T, SW><<<grid, kThreads, smem, stream>>>(P);
+    return cudaGetLastError();
 }
 
 template <typename T>
@@ -643,7 +712,6 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
     P.y = y;
     P.C_out = (int)p.C_out;
     P.n_kblk = pl.C_pad / kBlockK;
-    P.n_tile = pl.n_tile;
     P.n_oc_tiles = pl.n_oc_tiles;
     for (int a = 0; a < 3; ++a) {
         P.O[a] = (int)p.O[a];
@@ -657,22 +725,24 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
             }
         }
     }
+    P.NP = pl.NP;
     P.WC = pl.WC;
     P.MR = pl.MR;
-    P.sw = pl.sw;
     for (int r = 0; r < pl.sw; ++r) P.qw_ext[r] = (int)pl.ax[2].q_extent[r];
     P.stages = pl.stages;
     P.a_bytes = kBlockM * 128;
-    P.stage_bytes = P.a_bytes + pl.n_tile * 128;
-    P.acc_stride = pl.sw * pl.n_tile;
+    P.stage_bytes = (uint32_t)pl.stage_bytes;
+    P.acc_stride = pl.sw * pl.NP;
+    P.n_buf = pl.n_buf;
     uint32_t cols = 32;
-    while (cols < (uint32_t)(2 * P.acc_stride)) cols *= 2;
+    while (cols < (uint32_t)(pl.n_buf * P.acc_stride)) cols *= 2;
     P.tmem_cols = cols;
     P.idesc = (1u << 4)                                   // D = f32
               | ((p.dtype == CT_BF16 ? 1u : 0u) << 7)     // A = bf16 / f16
               | ((p.dtype == CT_BF16 ? 1u : 0u) << 10)    // B = bf16 / f16
-              | ((uint32_t)(pl.n_tile >> 3) << 17)        // N
-              | ((uint32_t)(kBlockM >> 4) << 24);         // M
+              | ((uint32_t)(pl.NP >> 3) << 17)            // N = positions
+              | ((uint32_t)(kBlockM >> 4) << 24);         // M = output channels
+    P.vec_store = (p.O[2] % 8 == 0) && ((uintptr_t)y % 16 == 0);
 
     // ---- tile classes, heaviest first (longest-processing-time order)
     TcClass hc[kTcMaxClasses];
@@ -691,14 +761,16 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
             c.n_qw_blk = qw_blk;
             c.qd_ext = (int)qd;
             c.qh_ext = (int)qh;
-            c.count = (int)(p.B * c.n_qd * c.n_qh_blk * c.n_qw_blk * pl.n_oc_tiles);
+            const int64_t cnt = p.B * c.n_qd * (int64_t)c.n_qh_blk * c.n_qw_blk * pl.n_oc_tiles;
+            if (cnt >= (1ll << 31)) return cudaErrorInvalidValue;
+            c.count = (int)cnt;
             int wsum = 0;
             for (int rw = 0; rw < pl.sw; ++rw)
                 wsum += pl.ax[0].ntaps[rd] * pl.ax[1].ntaps[rh] * pl.ax[2].ntaps[rw];
             work[n] = wsum;
             hc[n++] = c;
         }
-    for (int i = 0; i < n; ++i)  // stable selection sort, descending work
+    for (int i = 0; i < n; ++i)  // selection sort, descending work
         for (int j = i + 1; j < n; ++j)
             if (work[j] > work[i]) {
                 std::swap(work[i], work[j]);
@@ -720,6 +792,18 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
     const CUtensorMapDataType dt =
         p.dtype == CT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     {
+        const cuuint64_t dims[3] = {(cuuint64_t)pl.C_pad, (cuuint64_t)pl.N_pad,
+                                    (cuuint64_t)p.taps()};
+        const cuuint64_t strides[2] = {(cuuint64_t)pl.C_pad * 2,
+                                       (cuuint64_t)pl.C_pad * 2 * pl.N_pad};
+        const cuuint32_t box[3] = {(cuuint32_t)kBlockK, (cuuint32_t)kBlockM, 1};
+        const cuuint32_t es[3] = {1, 1, 1};
+        CUresult r = enc(&P.tmap_w, dt, 3, wp, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    {
         const cuuint64_t dims[5] = {(cuuint64_t)pl.C_pad, (cuuint64_t)p.I[2], (cuuint64_t)p.I[1],
                                     (cuuint64_t)p.I[0], (cuuint64_t)p.B};
         const cuuint64_t row = (cuuint64_t)pl.C_pad * 2;
@@ -727,19 +811,7 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
                                        row * p.I[2] * p.I[1] * p.I[0]};
         const cuuint32_t box[5] = {(cuuint32_t)kBlockK, (cuuint32_t)pl.WC, (cuuint32_t)pl.MR, 1, 1};
         const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-        CUresult r = enc(&P.tmap_a, dt, 5, xc, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    }
-    {
-        const cuuint64_t dims[3] = {(cuuint64_t)pl.C_pad, (cuuint64_t)pl.N_pad,
-                                    (cuuint64_t)p.taps()};
-        const cuuint64_t strides[2] = {(cuuint64_t)pl.C_pad * 2,
-                                       (cuuint64_t)pl.C_pad * 2 * pl.N_pad};
-        const cuuint32_t box[3] = {(cuuint32_t)kBlockK, (cuuint32_t)pl.n_tile, 1};
-        const cuuint32_t es[3] = {1, 1, 1};
-        CUresult r = enc(&P.tmap_b, dt, 3, wp, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+        CUresult r = enc(&P.tmap_x, dt, 5, xc, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
@@ -767,15 +839,17 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     const size_t smem = (size_t)P.stages * P.stage_bytes + 1024;
-    e = cudaFuncSetAttribute(tc_phase_gemm<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e != cudaSuccess) return e;
     const int grid = std::max(1, std::min(P.total_tiles, dev.sm_count));
     prof_begin(prof, stream);
-    tc_phase_gemm<T><<<grid, kThreads, smem, stream>>>(P);
+    switch (pl.sw) {
+        case 1: e = launch_gemm<T, 1>(P, grid, smem, stream); break;
+        case 2: e = launch_gemm<T, 2>(P, grid, smem, stream); break;
+        case 3: e = launch_gemm<T, 3>(P, grid, smem, stream); break;
+        default: e = launch_gemm<T, 4>(P, grid, smem, stream); break;
+    }
     prof_end(prof, stream);
     prof_count(prof);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace
