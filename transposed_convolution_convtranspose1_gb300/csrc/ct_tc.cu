@@ -63,7 +63,8 @@ constexpr int kTcMaxTaps = 8;     // taps per axis and phase on this route
 constexpr int kTcMaxClasses = 32; // (D residue, H residue) classes
 constexpr int kBlockM = 128;      // output channels per tile (TMEM lanes)
 constexpr int kBlockK = 64;       // channels per k-block (one 128-byte row)
-constexpr int kThreads = 192;     // 6 warps
+constexpr int kEpiWarps = 8;      // epilogue warps (two per TMEM lane quarter)
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer + MMA + epilogue warps
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait before giving up
 
 // Error codes in g_device_error (bit flags).
@@ -82,7 +83,6 @@ struct TcClass {
 struct TcParams {
     CUtensorMap tmap_w;   // W' [taps][N_pad][C_pad] as 3-D (C_pad, N_pad, taps)
     CUtensorMap tmap_x;   // X' [B, D, H, W, C_pad] as 5-D (C_pad, W, H, D, B)
-    CUtensorMap tmap_y;   // y [B, C_out, O_d, O_h, O_w] as 5-D (O_w, O_h, O_d, C_out, B)
     const void* bias;
     void* y;
     int C_out, n_kblk, n_oc_tiles;
@@ -101,11 +101,7 @@ struct TcParams {
     uint32_t stage_bytes, a_bytes;
     uint32_t idesc;
     uint32_t tmem_cols;
-    int acc_stride;       // TMEM columns per accumulator buffer (sw * NP)
-    int n_buf;            // accumulator buffers (1 or 2)
     int vec_store;        // 16-byte output stores allowed (O_w % 8 == 0, y aligned)
-    int tma_store;        // epilogue writes through tmap_y (64 outputs x 32 channels)
-    uint32_t epi_off;     // offset of the epilogue staging buffers from the ring
 };
 
 // ---------------------------------------------------------------------------
@@ -194,26 +190,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
-}
-
-__device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, uint32_t src, int c0, int c1,
-                                             int c2, int c3, int c4) {
-    asm volatile(
-        "cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4, %5}], [%6];" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(src)
-        : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Waits until at most N bulk stores of this thread still read shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -329,14 +305,38 @@ __device__ __forceinline__ bool tile_has_work(const TcParams& P, const Tile& T) 
     return false;
 }
 
+// Tile shape as a function of the W stride SW.
+template <int SW>
+struct TcShape {
+    static constexpr int NP = SW <= 2 ? 256 : 128;     // positions per tile (MMA N)
+    static constexpr int NSLOT = SW == 1 ? 2 : SW;     // accumulator slots of NP columns
+    static constexpr int NPW = NP / 2;                 // positions per epilogue warp
+    static constexpr int CQ = 32;                      // positions per TMEM load
+    static constexpr int NCH = NPW / CQ;               // chunks per epilogue warp
+};
+
+__device__ __forceinline__ uint32_t bits16(__nv_bfloat16 v) {
+    return *reinterpret_cast<const uint16_t*>(&v);
+}
+__device__ __forceinline__ uint32_t bits16(__half v) { return *reinterpret_cast<const uint16_t*>(&v); }
+
 // ---------------------------------------------------------------------------
 // the GEMM kernel; SW = W stride (W phases per tile)
+//
+// TMEM holds TcShape<SW>::NSLOT accumulator slots of NP columns.  For SW = 1
+// the two slots alternate between tiles (double buffering).  For SW >= 2 slot
+// rw holds W phase rw of the current tile; the MMA warp fills the slots in
+// phase order and the epilogue converts phases 0..SW-2 to packed 16-bit
+// outputs held in registers as soon as each is complete, releasing its slot
+// while the later phases' MMAs run; the last phase is combined with them and
+// stored while the next tile's first phases run.
 // ---------------------------------------------------------------------------
 
 template <typename T, int SW>
 __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_constant__ TcParams P) {
+    using Sh = TcShape<SW>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ uint64_t full_bar[8], empty_bar[8], tfull_bar[2], tempty_bar[2], drain_bar;
+    __shared__ uint64_t full_bar[8], empty_bar[8], sfull_bar[4], sempty_bar[4], drain_bar;
     __shared__ uint32_t tmem_base_slot;
     __shared__ volatile int abort_flag;
 
@@ -351,9 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&tfull_bar[b]), 1);
-            mbar_init(smem_u32(&tempty_bar[b]), 128);
+        for (int b = 0; b < 4; ++b) {
+            mbar_init(smem_u32(&sfull_bar[b]), 1);
+            mbar_init(smem_u32(&sempty_bar[b]), kEpiWarps * 32);
         }
         mbar_init(smem_u32(&drain_bar), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -432,27 +432,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
         // Lane 0 waits and issues; the other lanes wait at the final barrier.
         if (lane == 0) {
             int stage = 0;
-            uint32_t phase = 0, acc_iter = 0;
+            uint32_t phase = 0, work_iter = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
                 const Tile tl = decode_tile(P, t);
                 if (!tile_has_work<SW>(P, tl)) continue;
-                const int buf = P.n_buf == 2 ? (int)(acc_iter & 1) : 0;
-                const uint32_t tpar = (P.n_buf == 2 ? (acc_iter >> 1) : acc_iter) & 1;
-                if (!mbar_wait(smem_u32(&tempty_bar[buf]), tpar ^ 1, kErrMma, &abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
                 for (int rw = 0; rw < SW && ok; ++rw) {
+                    const int slot = SW == 1 ? (int)(work_iter & 1) : rw;
+                    const uint32_t use = SW == 1 ? (work_iter >> 1) : work_iter;
+                    if (!mbar_wait(smem_u32(&sempty_bar[slot]), (use & 1) ^ 1, kErrMma,
+                                   &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                     const int nk = phase_taps<SW>(P, tl, rw) * P.n_kblk;
-                    const uint32_t d = tmem_base + buf * P.acc_stride + rw * P.NP;
+                    const uint32_t d = tmem_base + slot * Sh::NP;
                     for (int j = 0; j < nk; ++j) {
                         if (!mbar_wait(smem_u32(&full_bar[stage]), phase, kErrMma, &abort_flag)) {
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
                         const uint32_t sa = ring + stage * P.stage_bytes;
                         const uint64_t ad = smem_desc_sw128(sa);
                         const uint64_t bd = smem_desc_sw128(sa + P.a_bytes);
@@ -467,10 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                             phase ^= 1;
                         }
                     }
+                    if (!ok) break;
+                    mma_commit(smem_u32(&sfull_bar[slot]));
                 }
-                if (!ok) break;
-                mma_commit(smem_u32(&tfull_bar[buf]));
-                ++acc_iter;
+                ++work_iter;
             }
             // no MMA may be in flight when TMEM is released
             mma_commit(smem_u32(&drain_bar));
@@ -479,124 +479,133 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        // Warp q (= warp % 4, the TMEM lane quarter it may read) owns output
-        // channels oc0 + 32q .. +31, one per lane.  Per chunk of CQ positions
-        // of one output row, each lane loads its channel's accumulators of all
-        // SW W phases, interleaves them (output s_w*q + rw), adds the bias,
-        // rounds once and writes its SW*CQ consecutive outputs with 16-byte
-        // stores.
-        constexpr int CQ = SW <= 2 ? 32 : 16;   // positions per chunk
-        constexpr int kPieces = SW * CQ / 8;    // 16-byte pieces per lane and chunk
+        // Warp e = warp - 2 reads TMEM lane quarter q = warp % 4 (output
+        // channels oc0 + 32q .. +31, one per lane) and positions
+        // [h * NPW, (h + 1) * NPW) of the tile, h = e / 4.
         const int q = warp & 3;
+        const int base = ((warp - 2) >> 2) * Sh::NPW;
         const T* __restrict__ bias = static_cast<const T*>(P.bias);
         T* __restrict__ y = static_cast<T*>(P.y);
-        uint32_t acc_iter = 0;
-        int ebuf = 0;
-        for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x) {
+        uint32_t work_iter = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
             const Tile Tl = decode_tile(P, t);
             const TcClass& C = P.cls[Tl.cls];
             const bool work = tile_has_work<SW>(P, Tl);
-            const int buf = P.n_buf == 2 ? (int)(acc_iter & 1) : 0;
-            if (work) {
-                const uint32_t tpar = (P.n_buf == 2 ? (acc_iter >> 1) : acc_iter) & 1;
-                const bool ok = __all_sync(
-                    0xffffffffu,
-                    mbar_wait(smem_u32(&tfull_bar[buf]), tpar, kErrEpilogue, &abort_flag));
-                if (!ok) break;
-                tc_fence_after();
-            }
             const int oc = Tl.oc0 + q * 32 + lane;
             const bool oc_ok = oc < P.C_out;
             const float bv = (bias != nullptr && oc_ok) ? to_f32(bias[oc]) : 0.f;
             const int od = Tl.rd + P.S[0] * Tl.qd;
             const bool d_ok = Tl.qd < C.qd_ext;
             const int64_t chan_base = ((int64_t)Tl.b * P.C_out + oc) * P.O[0] + od;
-            for (int p0 = 0; p0 < P.NP; p0 += CQ) {
-                const int row = p0 / P.WC;
-                const int qh = Tl.qh0 + row;
-                const int qwb = Tl.qw0 + (p0 % P.WC);
-                // warp-uniform: the chunk's positions are the same for every lane
-                if (!d_ok || qh >= C.qh_ext || qwb >= P.qw_ext[0]) continue;
-                const int oh = Tl.rh + P.S[1] * qh;
-                float v[SW][CQ];
+            const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
+            // chunk c covers positions base + 32c .. +31 of one output row
+            auto chunk_valid = [&](int c, int& oh, int& qwb) {
+                const int p0 = base + c * Sh::CQ;
+                const int qh = Tl.qh0 + p0 / P.WC;
+                qwb = Tl.qw0 + (p0 % P.WC);
+                oh = Tl.rh + P.S[1] * qh;
+                return d_ok && qh < C.qh_ext && qwb < P.qw_ext[0];
+            };
+
+            uint32_t held[SW > 1 ? SW - 1 : 1][Sh::NPW / 2];  // packed 16-bit outputs
+            // phases 0 .. SW-2 (SW >= 2): convert and hold, release the slot
 #pragma unroll
-                for (int rw = 0; rw < SW; ++rw) {
-                    if (work && phase_taps<SW>(P, Tl, rw) > 0) {
-                        const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) +
-                                            (uint32_t)(buf * P.acc_stride + rw * P.NP + p0);
-                        if constexpr (CQ == 32) tmem_ld32(ta, v[rw]);
-                        else tmem_ld16(ta, v[rw]);
+            for (int rw = 0; rw < SW - 1; ++rw) {
+                const bool has = work && phase_taps<SW>(P, Tl, rw) > 0;
+                if (work) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sfull_bar[rw]), work_iter & 1,
+                                                           kErrEpilogue, &abort_flag));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int c = 0; c < Sh::NCH; ++c) {
+                    int oh, qwb;
+                    float v[Sh::CQ];
+                    if (has && chunk_valid(c, oh, qwb)) {
+                        tmem_ld32(lane_addr + (uint32_t)(rw * Sh::NP + base + c * Sh::CQ), v);
+                        tmem_ld_wait();
                     } else {
 #pragma unroll
-                        for (int i = 0; i < CQ; ++i) v[rw][i] = 0.f;
+                        for (int i = 0; i < Sh::CQ; ++i) v[i] = 0.f;
                     }
+#pragma unroll
+                    for (int i = 0; i < Sh::CQ / 2; ++i)
+                        held[rw][c * (Sh::CQ / 2) + i] = bits16(from_f32<T>(v[2 * i] + bv)) |
+                                                         (bits16(from_f32<T>(v[2 * i + 1] + bv)) << 16);
                 }
-                tmem_ld_wait();
-                const int ow0 = SW * qwb;
-                if constexpr (SW * CQ == 64) {
-                    if (P.tma_store) {
-                        // stage the warp's 32 channels x 64 outputs (128-byte rows,
-                        // 128-byte swizzle) and write them with one tensor store;
-                        // the store clips outputs outside y.
-                        const uint32_t sbuf = ring + P.epi_off + (uint32_t)(q * 2 + ebuf) * 4096u;
-                        if (lane == 0) bulk_wait_read<1>();  // the store that used sbuf is done
-                        __syncwarp();
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            uint32_t wv[4];
-#pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                const int j0 = c * 8 + 2 * h, j1 = j0 + 1;
-                                const T lo = from_f32<T>(v[j0 % SW][j0 / SW] + bv);
-                                const T hi = from_f32<T>(v[j1 % SW][j1 / SW] + bv);
-                                wv[h] = (uint32_t)(*reinterpret_cast<const uint16_t*>(&lo)) |
-                                        ((uint32_t)(*reinterpret_cast<const uint16_t*>(&hi)) << 16);
-                            }
-                            const uint32_t a = sbuf + lane * 128 + ((c ^ (lane & 7)) << 4);
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(wv[0]),
-                                         "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
-                                         : "memory");
-                        }
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                        __syncwarp();
-                        if (lane == 0 && Tl.oc0 + q * 32 < P.C_out)  // no store starts outside y
-                            tma_store_5d(&P.tmap_y, sbuf, ow0, oh, od, Tl.oc0 + q * 32, Tl.b);
-                        ebuf ^= 1;
-                        continue;
-                    }
-                }
-                if (!oc_ok) continue;
-                T* dst = y + (chan_base * P.O[1] + oh) * (int64_t)P.O[2] + ow0;
-#pragma unroll
-                for (int c = 0; c < kPieces; ++c) {
-                    uint32_t wv[4];
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const int j0 = c * 8 + 2 * h, j1 = j0 + 1;  // output j = qi*SW + rw
-                        const T lo = from_f32<T>(v[j0 % SW][j0 / SW] + bv);
-                        const T hi = from_f32<T>(v[j1 % SW][j1 / SW] + bv);
-                        wv[h] = (uint32_t)(*reinterpret_cast<const uint16_t*>(&lo)) |
-                                ((uint32_t)(*reinterpret_cast<const uint16_t*>(&hi)) << 16);
-                    }
-                    const int ow = ow0 + c * 8;
-                    if (P.vec_store && ow + 8 <= P.O[2]) {
-                        *reinterpret_cast<uint4*>(dst + c * 8) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                    } else {
-                        uint16_t* d16 = reinterpret_cast<uint16_t*>(dst + c * 8);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            if (ow + i < P.O[2]) d16[i] = (uint16_t)(wv[i >> 1] >> (16 * (i & 1)));
-                    }
+                if (work) {
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&sempty_bar[rw]));
                 }
             }
-            if (work) {
-                tc_fence_before();
-                mbar_arrive(smem_u32(&tempty_bar[buf]));
-                ++acc_iter;
+            if (!ok) break;
+            // last phase (all of it for SW = 1): combine and store
+            {
+                const int rl = SW - 1;
+                const int slot = SW == 1 ? (int)(work_iter & 1) : rl;
+                const uint32_t use = SW == 1 ? (work_iter >> 1) : work_iter;
+                const bool has = work && phase_taps<SW>(P, Tl, rl) > 0;
+                if (work) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sfull_bar[slot]), use & 1,
+                                                           kErrEpilogue, &abort_flag));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int c = 0; c < Sh::NCH; ++c) {
+                    int oh, qwb;
+                    if (!chunk_valid(c, oh, qwb)) continue;  // warp-uniform
+                    float v[Sh::CQ];
+                    if (has) {
+                        tmem_ld32(lane_addr + (uint32_t)(slot * Sh::NP + base + c * Sh::CQ), v);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < Sh::CQ; ++i) v[i] = 0.f;
+                    }
+                    if (!oc_ok) continue;
+                    const int ow0 = SW * qwb;
+                    T* dst = y + (chan_base * P.O[1] + oh) * (int64_t)P.O[2] + ow0;
+                    // outputs j = qi * SW + r of this chunk, 8 per 16-byte piece
+#pragma unroll
+                    for (int pc = 0; pc < SW * Sh::CQ / 8; ++pc) {
+                        uint32_t wv[4];
+#pragma unroll
+                        for (int hh = 0; hh < 4; ++hh) {
+                            uint32_t two[2];
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int j = pc * 8 + hh * 2 + e;
+                                const int qi = j / SW, r = j % SW;
+                                if (r == SW - 1) {
+                                    two[e] = bits16(from_f32<T>(v[qi] + bv));
+                                } else {
+                                    const uint32_t w2 = held[r < SW - 1 ? r : 0][c * (Sh::CQ / 2) + qi / 2];
+                                    two[e] = (qi & 1) ? (w2 >> 16) : (w2 & 0xFFFFu);
+                                }
+                            }
+                            wv[hh] = two[0] | (two[1] << 16);
+                        }
+                        const int ow = ow0 + pc * 8;
+                        if (P.vec_store && ow + 8 <= P.O[2]) {
+                            *reinterpret_cast<uint4*>(dst + pc * 8) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                        } else {
+                            uint16_t* d16 = reinterpret_cast<uint16_t*>(dst + pc * 8);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                if (ow + i < P.O[2]) d16[i] = (uint16_t)(wv[i >> 1] >> (16 * (i & 1)));
+                        }
+                    }
+                }
+                if (work) {
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&sempty_bar[slot]));
+                    ++work_iter;
+                }
             }
         }
-        if (lane == 0) bulk_wait_all();  // tensor stores done before the CTA exits
-        __syncwarp();
     }
 
     tc_fence_before();
@@ -686,8 +695,8 @@ __global__ void __launch_bounds__(256) tc_channels_last(const T* __restrict__ x,
 // ---------------------------------------------------------------------------
 
 struct TcPlan {
-    int C_pad, N_pad, n_oc_tiles, sw, NP, WC, MR, stages, n_buf;
-    size_t x_bytes, w_bytes, epi_bytes, stage_bytes;
+    int C_pad, N_pad, n_oc_tiles, sw, NP, WC, MR, stages, nslot;
+    size_t x_bytes, w_bytes, stage_bytes;
     AxisPlan ax[3];
 };
 
@@ -704,9 +713,8 @@ bool make_plan(const Problem& p, TcPlan* pl) {
     }
     if (p.S[0] * p.S[1] > kTcMaxClasses) return false;
     pl->sw = p.S[2];
-    pl->NP = pl->sw <= 2 ? 256 : 128;
-    const int acc_stride = pl->sw * pl->NP;
-    pl->n_buf = 2 * acc_stride <= 512 ? 2 : 1;
+    pl->NP = pl->sw <= 2 ? 256 : 128;      // TcShape<SW>::NP
+    pl->nslot = pl->sw == 1 ? 2 : pl->sw;  // TcShape<SW>::NSLOT
     pl->N_pad = (int)((p.C_out + kBlockM - 1) / kBlockM * kBlockM);
     pl->n_oc_tiles = pl->N_pad / kBlockM;
     pl->C_pad = (int)((p.C_in + kBlockK - 1) / kBlockK * kBlockK);
@@ -716,9 +724,7 @@ bool make_plan(const Problem& p, TcPlan* pl) {
     pl->WC = wc;
     pl->MR = pl->NP / wc;
     pl->stage_bytes = (size_t)kBlockM * 128 + (size_t)pl->NP * 128;
-    // epilogue staging for tensor stores: 4 warps x 2 buffers x 4 KiB
-    pl->epi_bytes = (pl->sw == 2 || pl->sw == 4) ? 4 * 2 * 4096 : 0;
-    const size_t room = kSmemLimit - 1024 - pl->epi_bytes - 1024;
+    const size_t room = kSmemLimit - 1024 - 1024;
     pl->stages = (int)std::min<size_t>(8, room / pl->stage_bytes);
     if (pl->stages < 2) return false;
     pl->x_bytes = (size_t)p.B * p.in_spatial() * pl->C_pad * 2;
@@ -791,10 +797,8 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
     P.stages = pl.stages;
     P.a_bytes = kBlockM * 128;
     P.stage_bytes = (uint32_t)pl.stage_bytes;
-    P.acc_stride = pl.sw * pl.NP;
-    P.n_buf = pl.n_buf;
     uint32_t cols = 32;
-    while (cols < (uint32_t)(pl.n_buf * P.acc_stride)) cols *= 2;
+    while (cols < (uint32_t)(pl.nslot * pl.NP)) cols *= 2;
     P.tmem_cols = cols;
     P.idesc = (1u << 4)                                   // D = f32
               | ((p.dtype == CT_BF16 ? 1u : 0u) << 7)     // A = bf16 / f16
@@ -802,8 +806,6 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
               | ((uint32_t)(pl.NP >> 3) << 17)            // N = positions
               | ((uint32_t)(kBlockM >> 4) << 24);         // M = output channels
     P.vec_store = (p.O[2] % 8 == 0) && ((uintptr_t)y % 16 == 0);
-    P.tma_store = P.vec_store && pl.epi_bytes > 0 && p.C_out <= (1ll << 31) / 2;
-    P.epi_off = (uint32_t)(pl.stages * pl.stage_bytes);
 
     // ---- tile classes, heaviest first (longest-processing-time order)
     TcClass hc[kTcMaxClasses];
@@ -878,20 +880,6 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
 
-    if (P.tma_store) {
-        const cuuint64_t dims[5] = {(cuuint64_t)p.O[2], (cuuint64_t)p.O[1], (cuuint64_t)p.O[0],
-                                    (cuuint64_t)p.C_out, (cuuint64_t)p.B};
-        const cuuint64_t row = (cuuint64_t)p.O[2] * 2;
-        const cuuint64_t strides[4] = {row, row * p.O[1], row * p.O[1] * p.O[0],
-                                       row * p.O[1] * p.O[0] * p.C_out};
-        const cuuint32_t box[5] = {64, 1, 1, 32, 1};
-        const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-        CUresult r = enc(&P.tmap_y, dt, 5, y, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    }
-
     // ---- launches
     {
         const int64_t tot = p.taps() * pl.N_pad * pl.C_pad;
@@ -913,7 +901,7 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
         prof_count(prof);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    const size_t smem = (size_t)P.stages * P.stage_bytes + pl.epi_bytes + 1024;
+    const size_t smem = (size_t)P.stages * P.stage_bytes + 1024;
     const int grid = std::max(1, std::min(P.total_tiles, dev.sm_count));
     prof_begin(prof, stream);
     switch (pl.sw) {
