@@ -83,6 +83,7 @@ struct TcClass {
 struct TcParams {
     CUtensorMap tmap_w;   // W' [taps][N_pad][C_pad] as 3-D (C_pad, N_pad, taps)
     CUtensorMap tmap_x;   // X' [B, D, H, W, C_pad] as 5-D (C_pad, W, H, D, B)
+    CUtensorMap tmap_y;   // y [B, C_out, O_d, O_h, O_w] as 5-D (O_w, O_h, O_d, C_out, B)
     const void* bias;
     void* y;
     int C_out, n_kblk, n_oc_tiles;
@@ -102,6 +103,8 @@ struct TcParams {
     uint32_t idesc;
     uint32_t tmem_cols;
     int vec_store;        // 16-byte output stores allowed (O_w % 8 == 0, y aligned)
+    int tma_store;        // SW = 2: epilogue writes 32 channels x 64 outputs per tensor store
+    uint32_t epi_off;     // offset of the per-warp 4 KiB staging buffers from the ring
 };
 
 // ---------------------------------------------------------------------------
@@ -190,6 +193,25 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
+}
+
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4, %5}], [%6];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(src)
+        : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until no bulk store of this thread still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -565,8 +587,38 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
 #pragma unroll
                         for (int i = 0; i < Sh::CQ; ++i) v[i] = 0.f;
                     }
-                    if (!oc_ok) continue;
                     const int ow0 = SW * qwb;
+                    if constexpr (SW == 2) {
+                        if (P.tma_store) {
+                            // stage 32 channels x 64 outputs (128-byte rows, 128-byte
+                            // swizzle) and write them with one tensor store, which
+                            // clips outputs outside y
+                            const uint32_t sbuf = ring + P.epi_off + (uint32_t)(warp - 2) * 4096u;
+                            if (lane == 0) bulk_wait_read_all();  // previous store left sbuf
+                            __syncwarp();
+#pragma unroll
+                            for (int pc = 0; pc < 8; ++pc) {
+                                uint32_t wv[4];
+#pragma unroll
+                                for (int hh = 0; hh < 4; ++hh) {
+                                    const int qi = pc * 4 + hh;  // outputs 2qi (phase 0), 2qi+1
+                                    const uint32_t w2 = held[0][c * (Sh::CQ / 2) + qi / 2];
+                                    const uint32_t lo = (qi & 1) ? (w2 >> 16) : (w2 & 0xFFFFu);
+                                    wv[hh] = lo | (bits16(from_f32<T>(v[qi] + bv)) << 16);
+                                }
+                                const uint32_t a = sbuf + lane * 128 + ((pc ^ (lane & 7)) << 4);
+                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                                             "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
+                                             : "memory");
+                            }
+                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                            __syncwarp();
+                            if (lane == 0 && Tl.oc0 + q * 32 < P.C_out)  // starts inside y
+                                tma_store_5d(&P.tmap_y, sbuf, ow0, oh, od, Tl.oc0 + q * 32, Tl.b);
+                            continue;
+                        }
+                    }
+                    if (!oc_ok) continue;
                     T* dst = y + (chan_base * P.O[1] + oh) * (int64_t)P.O[2] + ow0;
                     // outputs j = qi * SW + r of this chunk, 8 per 16-byte piece
 #pragma unroll
@@ -606,6 +658,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                 }
             }
         }
+        if (lane == 0) bulk_wait_all();  // tensor stores complete before the CTA exits
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -696,7 +750,7 @@ __global__ void __launch_bounds__(256) tc_channels_last(const T* __restrict__ x,
 
 struct TcPlan {
     int C_pad, N_pad, n_oc_tiles, sw, NP, WC, MR, stages, nslot;
-    size_t x_bytes, w_bytes, stage_bytes;
+    size_t x_bytes, w_bytes, stage_bytes, epi_bytes;
     AxisPlan ax[3];
 };
 
@@ -724,7 +778,9 @@ bool make_plan(const Problem& p, TcPlan* pl) {
     pl->WC = wc;
     pl->MR = pl->NP / wc;
     pl->stage_bytes = (size_t)kBlockM * 128 + (size_t)pl->NP * 128;
-    const size_t room = kSmemLimit - 1024 - 1024;
+    // SW = 2 epilogue: one 4 KiB tensor-store staging buffer per epilogue warp
+    pl->epi_bytes = pl->sw == 2 ? (size_t)kEpiWarps * 4096 : 0;
+    const size_t room = kSmemLimit - 1024 - 1024 - pl->epi_bytes;
     pl->stages = (int)std::min<size_t>(8, room / pl->stage_bytes);
     if (pl->stages < 2) return false;
     pl->x_bytes = (size_t)p.B * p.in_spatial() * pl->C_pad * 2;
@@ -806,6 +862,8 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
               | ((uint32_t)(pl.NP >> 3) << 17)            // N = positions
               | ((uint32_t)(kBlockM >> 4) << 24);         // M = output channels
     P.vec_store = (p.O[2] % 8 == 0) && ((uintptr_t)y % 16 == 0);
+    P.tma_store = P.vec_store && pl.epi_bytes > 0;
+    P.epi_off = (uint32_t)(pl.stages * pl.stage_bytes);
 
     // ---- tile classes, heaviest first (longest-processing-time order)
     TcClass hc[kTcMaxClasses];
@@ -880,6 +938,20 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
 
+    if (P.tma_store) {
+        const cuuint64_t dims[5] = {(cuuint64_t)p.O[2], (cuuint64_t)p.O[1], (cuuint64_t)p.O[0],
+                                    (cuuint64_t)p.C_out, (cuuint64_t)p.B};
+        const cuuint64_t row = (cuuint64_t)p.O[2] * 2;
+        const cuuint64_t strides[4] = {row, row * p.O[1], row * p.O[1] * p.O[0],
+                                       row * p.O[1] * p.O[0] * p.C_out};
+        const cuuint32_t box[5] = {64, 1, 1, 32, 1};
+        const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+        CUresult r = enc(&P.tmap_y, dt, 5, y, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+
     // ---- launches
     {
         const int64_t tot = p.taps() * pl.N_pad * pl.C_pad;
@@ -901,7 +973,7 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
         prof_count(prof);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    const size_t smem = (size_t)P.stages * P.stage_bytes + 1024;
+    const size_t smem = (size_t)P.stages * P.stage_bytes + pl.epi_bytes + 1024;
     const int grid = std::max(1, std::min(P.total_tiles, dev.sm_count));
     prof_begin(prof, stream);
     switch (pl.sw) {
