@@ -15,6 +15,9 @@
 //     read once per (tap, channel) with lanes on consecutive positions;
 //   - stores: for each output channel a warp writes 32*s_w consecutive
 //     elements of one output row.
+// The staged variant (used whenever its shared-memory footprint fits) first
+// copies a band's input rows into shared memory; the direct variant reads
+// the input through the L1 cache.
 #include <algorithm>
 #include <cstring>
 
@@ -29,6 +32,7 @@ constexpr int kGrpMaxSA = 8;      // D / H stride
 constexpr int kGrpMaxTaps = 8;    // taps per axis and residue
 constexpr int kGrpWarps = 8;      // rows per block
 constexpr size_t kGrpMaxSlab = 48 * 1024;
+constexpr int kGrpStageW = 4;     // staged variant: input width <= 32 * kGrpStageW
 
 struct GroupedParams {
     const void* x;
@@ -43,6 +47,8 @@ struct GroupedParams {
     int qw_ext[kGrpMaxS];
     int n_rowblk;          // ceil(O_d * O_h / kGrpWarps)
     int taps;              // kD * kH * kW
+    // staged variant: bands of R output rows of one output depth
+    int R, n_band, nr_max, offmin_h;
 };
 
 // slab layout: [tap][ic][COG] (COG >= Cog, zero padded)
@@ -136,10 +142,164 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_kernel(const __grid_co
     }
 }
 
+
+// Staged variant: one block per (b, g, od, band of R output rows).  The input
+// rows the band reads (every D tap of the depth's phase, the H rows of all the
+// band's rows, all Cig channels, the full W extent) are first copied into
+// shared memory with coalesced loads (zeros outside the input), so the
+// gather itself reads only shared memory.  Each lane then owns two q
+// positions of a row (q and q + 32) and every W residue of them.
+template <typename T, int SW, int COG>
+__global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __grid_constant__ GroupedParams P) {
+    extern __shared__ float sm[];
+    const T* __restrict__ x = static_cast<const T*>(P.x);
+    const T* __restrict__ w = static_cast<const T*>(P.w);
+    const T* __restrict__ bias = static_cast<const T*>(P.bias);
+    T* __restrict__ y = static_cast<T*>(P.y);
+
+    int64_t blk = blockIdx.x;
+    const int band = (int)(blk % P.n_band); blk /= P.n_band;
+    const int od = (int)(blk % P.O[0]); blk /= P.O[0];
+    const int g = (int)(blk % P.G);
+    const int64_t b = blk / P.G;
+    const int rd = od % P.S[0], qd = od / P.S[0];
+    const int nd_ = P.ntap[0][rd];
+    const int oh0 = band * P.R;
+    const int ih_lo = oh0 / P.S[1] + P.offmin_h;
+    const int NR = P.nr_max;
+    const int IW = P.I[2];
+
+    float* slab = sm;
+    float* xs = sm + P.taps * P.Cig * COG;
+    const int slab_n = P.taps * P.Cig * COG;
+    for (int e = threadIdx.x; e < slab_n; e += blockDim.x) {
+        const int oc = e % COG;
+        const int ic = (e / COG) % P.Cig;
+        const int t = e / (COG * P.Cig);
+        float v = 0.f;
+        if (oc < P.Cog) v = to_f32(w[((int64_t)(g * P.Cig + ic) * P.Cog + oc) * P.taps + t]);
+        slab[e] = v;
+    }
+    const int64_t in_plane = (int64_t)P.I[0] * P.I[1] * IW;
+    const T* xg = x + (b * P.C_in + (int64_t)g * P.Cig) * in_plane;
+    {
+        // one staged row (jd, ic, r) per warp iteration, lanes along W; four
+        // rows' loads are issued before any of them is stored
+        const int warp_s = threadIdx.x / 32, lane_s = threadIdx.x % 32;
+        const int nrows = nd_ * P.Cig * NR;
+        for (int r0 = warp_s * 4; r0 < nrows; r0 += kGrpWarps * 4) {
+            float v[4][kGrpStageW];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int rr = r0 + u;
+                const int r = rr % NR, ic = (rr / NR) % P.Cig, jd = rr / (NR * P.Cig);
+                const int id = rr < nrows ? qd + P.off[0][rd][jd] : -1;
+                const int ih = ih_lo + r;
+                const bool row_ok = rr < nrows && id >= 0 && id < P.I[0] && ih >= 0 && ih < P.I[1];
+                const T* src = xg + (int64_t)ic * in_plane + ((int64_t)id * P.I[1] + ih) * IW;
+#pragma unroll
+                for (int k = 0; k < kGrpStageW; ++k) {
+                    const int iw = lane_s + 32 * k;
+                    v[u][k] = (row_ok && iw < IW) ? to_f32(src[iw]) : 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (r0 + u >= nrows) break;
+#pragma unroll
+                for (int k = 0; k < kGrpStageW; ++k) {
+                    const int iw = lane_s + 32 * k;
+                    if (iw < IW) xs[(r0 + u) * IW + iw] = v[u][k];
+                }
+            }
+        }
+    }
+    __syncthreads();
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    float bv[COG];
+#pragma unroll
+    for (int oc = 0; oc < COG; ++oc)
+        bv[oc] = (bias != nullptr && oc < P.Cog) ? to_f32(bias[g * P.Cog + oc]) : 0.f;
+    const int64_t out_plane = (int64_t)P.O[0] * P.O[1] * P.O[2];
+    const int nq = P.qw_ext[0];
+    const int plane_rows = P.Cig * NR * IW;   // floats per D tap in xs
+
+    const int rows_per_warp = P.R / kGrpWarps;
+    for (int i = 0; i < rows_per_warp; ++i) {
+        const int row = warp * rows_per_warp + i;  // consecutive rows: mixed H residues
+        const int oh = oh0 + row;
+        if (oh >= P.O[1]) break;
+        const int rh = oh % P.S[1], qh = oh / P.S[1];
+        const int nh_ = P.ntap[1][rh];
+        T* yrow = y + (b * P.C_out + (int64_t)g * P.Cog) * out_plane +
+                  ((int64_t)od * P.O[1] + oh) * P.O[2];
+        for (int qb = 0; qb < nq; qb += 64) {
+            const int qv[2] = {qb + lane, qb + 32 + lane};
+            float acc[2][SW][COG];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int r = 0; r < SW; ++r)
+#pragma unroll
+                    for (int oc = 0; oc < COG; ++oc) acc[u][r][oc] = 0.f;
+#pragma unroll
+            for (int r = 0; r < SW; ++r) {
+                const int nw_ = P.ntap[2][r];
+                for (int jd = 0; jd < nd_; ++jd)
+                    for (int jh = 0; jh < nh_; ++jh) {
+                        const int lr = qh + P.off[1][rh][jh] - ih_lo;
+                        const float* xr = xs + jd * plane_rows + lr * IW;
+                        const int tdh = (P.tap[0][rd][jd] * P.Kdims[1] + P.tap[1][rh][jh]) * P.Kdims[2];
+                        for (int jw = 0; jw < nw_; ++jw) {
+                            const int ow_off = P.off[2][r][jw];
+                            const float* ws = slab + (tdh + P.tap[2][r][jw]) * P.Cig * COG;
+                            int iw[2];
+                            bool ok[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                iw[u] = qv[u] + ow_off;
+                                ok[u] = qv[u] < P.qw_ext[r] && iw[u] >= 0 && iw[u] < IW;
+                            }
+                            for (int ic = 0; ic < P.Cig; ++ic) {
+                                const float* wv = ws + ic * COG;
+                                const float x0 = ok[0] ? xr[ic * NR * IW + iw[0]] : 0.f;
+                                const float x1 = ok[1] ? xr[ic * NR * IW + iw[1]] : 0.f;
+#pragma unroll
+                                for (int oc = 0; oc < COG; ++oc) {
+                                    acc[0][r][oc] = fmaf(x0, wv[oc], acc[0][r][oc]);
+                                    acc[1][r][oc] = fmaf(x1, wv[oc], acc[1][r][oc]);
+                                }
+                            }
+                        }
+                    }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int q = qv[u];
+                if (q >= nq) continue;
+#pragma unroll
+                for (int oc = 0; oc < COG; ++oc) {
+                    if (oc >= P.Cog) break;
+                    T* yo = yrow + (int64_t)oc * out_plane + (int64_t)SW * q;
+#pragma unroll
+                    for (int r = 0; r < SW; ++r)
+                        if (q < P.qw_ext[r]) yo[r] = from_f32<T>(acc[u][r][oc] + bv[oc]);
+                }
+            }
+        }
+    }
+}
+
 struct GroupedPlan {
     AxisPlan ax[3];
     int cog_pad;
+    bool staged;
+    int R, nr_max, offmin_h;
+    size_t smem;
 };
+
+constexpr size_t kGrpMaxStaged = 96 * 1024;
 
 int pad_cog(int cog) {
     if (cog <= 1) return 1;
@@ -161,12 +321,47 @@ bool make_plan(const Problem& p, GroupedPlan* pl) {
     const size_t slab = (size_t)p.taps() * p.Cig * pl->cog_pad * sizeof(float);
     if (slab > kGrpMaxSlab) return false;
     if (p.O[0] * p.O[1] >= (1ll << 30)) return false;
+    // staged variant: bands of R rows; the band reads input rows
+    // [oh0 / s_h + min_off, (oh0 + R - 1) / s_h + max_off]
+    int offmin = 1 << 30, offmax = -(1 << 30), ndmax = 0;
+    for (int r = 0; r < p.S[1]; ++r)
+        for (int j = 0; j < pl->ax[1].ntaps[r]; ++j) {
+            offmin = std::min(offmin, pl->ax[1].off[r][j]);
+            offmax = std::max(offmax, pl->ax[1].off[r][j]);
+        }
+    for (int r = 0; r < p.S[0]; ++r) ndmax = std::max(ndmax, pl->ax[0].ntaps[r]);
+    pl->staged = false;
+    if (offmin <= offmax && p.I[2] <= 32 * kGrpStageW) {
+        for (int R : {16, 8}) {
+            // floor((oh0 + R - 1) / s) - floor(oh0 / s) <= floor((R - 1) / s) + 1
+            const int nr = (R - 1) / p.S[1] + 2 + (offmax - offmin);
+            const size_t sm = slab + (size_t)std::max(ndmax, 1) * p.Cig * nr * p.I[2] * sizeof(float);
+            if (sm <= kGrpMaxStaged) {
+                pl->staged = true;
+                pl->R = R;
+                pl->nr_max = nr;
+                pl->offmin_h = offmin;
+                pl->smem = sm;
+                break;
+            }
+        }
+    }
     return true;
 }
 
 template <typename T, int SW, int COG>
-cudaError_t launch_grouped_t(const GroupedParams& P, int64_t blocks, size_t slab, cudaStream_t stream) {
-    grouped_kernel<T, SW, COG><<<(unsigned)blocks, kGrpWarps * 32, slab, stream>>>(P);
+cudaError_t launch_grouped_t(const GroupedParams& P, int64_t blocks, size_t smem, cudaStream_t stream) {
+    if (P.R > 0) {
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(grouped_staged_kernel<T, SW, COG>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        grouped_staged_kernel<T, SW, COG><<<(unsigned)blocks, kGrpWarps * 32, smem, stream>>>(P);
+    } else {
+        grouped_kernel<T, SW, COG><<<(unsigned)blocks, kGrpWarps * 32, smem, stream>>>(P);
+    }
     return cudaGetLastError();
 }
 
@@ -233,9 +428,17 @@ cudaError_t launch_grouped(const Problem& p, const void* x, const void* w, const
     for (int r = 0; r < p.S[2]; ++r) P.qw_ext[r] = (int)pl.ax[2].q_extent[r];
     P.taps = (int)p.taps();
     P.n_rowblk = (int)((p.O[0] * p.O[1] + kGrpWarps - 1) / kGrpWarps);
-    const int64_t blocks = p.B * (int64_t)p.G * P.n_rowblk;
+    int64_t blocks = p.B * (int64_t)p.G * P.n_rowblk;
+    size_t slab = (size_t)P.taps * P.Cig * pl.cog_pad * sizeof(float);
+    if (pl.staged) {
+        P.R = pl.R;
+        P.n_band = (int)((p.O[1] + pl.R - 1) / pl.R);
+        P.nr_max = pl.nr_max;
+        P.offmin_h = pl.offmin_h;
+        blocks = p.B * (int64_t)p.G * p.O[0] * P.n_band;
+        slab = pl.smem;
+    }
     if (blocks >= (1ll << 31)) return cudaErrorInvalidConfiguration;
-    const size_t slab = (size_t)P.taps * P.Cig * pl.cog_pad * sizeof(float);
     prof_begin(prof, stream);
     cudaError_t e;
     switch (p.dtype) {
