@@ -49,6 +49,8 @@ struct GroupedParams {
     int taps;              // kD * kH * kW
     // staged variant: bands of R output rows of one output depth
     int R, n_band, nr_max, offmin_h;
+    int vec2;              // fp32, stride 2 along W: rows 8-byte aligned (float2 stores)
+    int cigp;              // staged variant: channels per group padded to 4, 8 or 16
 };
 
 // slab layout: [tap][ic][COG] (COG >= Cog, zero padded)
@@ -145,13 +147,15 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_kernel(const __grid_co
 
 // Staged variant: one block per (b, g, od, band of R output rows).  The input
 // rows the band reads (every D tap of the depth's phase, the H rows of all the
-// band's rows, all Cig channels, the full W extent) are first copied into
-// shared memory with coalesced loads (zeros outside the input), so the
-// gather itself reads only shared memory.  Each lane then owns two q
-// positions of a row (q and q + 32) and every W residue of them.
-template <typename T, int SW, int COG>
+// band's rows, the full W extent, the group's channels padded to CIGP) are
+// first copied into shared memory channels-innermost ([row][w][ic], zeros
+// outside the input), so that for one tap a lane reads its CIGP channels with
+// CIGP/4 16-byte loads at fixed offsets.  Each lane owns two q positions of a
+// row (q and q + 32) and every W residue of them; per tap the COG x CIGP
+// weights are loaded once (broadcast) and used for both positions.
+template <typename T, int SW, int COG, int CIGP>
 __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __grid_constant__ GroupedParams P) {
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float sm[];
     const T* __restrict__ x = static_cast<const T*>(P.x);
     const T* __restrict__ w = static_cast<const T*>(P.w);
     const T* __restrict__ bias = static_cast<const T*>(P.bias);
@@ -169,33 +173,35 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __
     const int NR = P.nr_max;
     const int IW = P.I[2];
 
+    // weights: slab[tap][ic][oc], CIGP x COG per tap (zero padded)
     float* slab = sm;
-    float* xs = sm + P.taps * P.Cig * COG;
-    const int slab_n = P.taps * P.Cig * COG;
+    float* xs = sm + P.taps * CIGP * COG;  // [jd][r][iw][CIGP]
+    const int slab_n = P.taps * CIGP * COG;
     for (int e = threadIdx.x; e < slab_n; e += blockDim.x) {
         const int oc = e % COG;
-        const int ic = (e / COG) % P.Cig;
-        const int t = e / (COG * P.Cig);
+        const int ic = (e / COG) % CIGP;
+        const int t = e / (COG * CIGP);
         float v = 0.f;
-        if (oc < P.Cog) v = to_f32(w[((int64_t)(g * P.Cig + ic) * P.Cog + oc) * P.taps + t]);
+        if (oc < P.Cog && ic < P.Cig)
+            v = to_f32(w[((int64_t)(g * P.Cig + ic) * P.Cog + oc) * P.taps + t]);
         slab[e] = v;
     }
     const int64_t in_plane = (int64_t)P.I[0] * P.I[1] * IW;
     const T* xg = x + (b * P.C_in + (int64_t)g * P.Cig) * in_plane;
     {
-        // one staged row (jd, ic, r) per warp iteration, lanes along W; four
-        // rows' loads are issued before any of them is stored
+        // one (jd, r, ic) input row per warp iteration, lanes along W
         const int warp_s = threadIdx.x / 32, lane_s = threadIdx.x % 32;
-        const int nrows = nd_ * P.Cig * NR;
+        const int nrows = nd_ * NR * CIGP;
         for (int r0 = warp_s * 4; r0 < nrows; r0 += kGrpWarps * 4) {
             float v[4][kGrpStageW];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int rr = r0 + u;
-                const int r = rr % NR, ic = (rr / NR) % P.Cig, jd = rr / (NR * P.Cig);
+                const int ic = rr % CIGP, r = (rr / CIGP) % NR, jd = rr / (CIGP * NR);
                 const int id = rr < nrows ? qd + P.off[0][rd][jd] : -1;
                 const int ih = ih_lo + r;
-                const bool row_ok = rr < nrows && id >= 0 && id < P.I[0] && ih >= 0 && ih < P.I[1];
+                const bool row_ok = rr < nrows && ic < P.Cig && id >= 0 && id < P.I[0] &&
+                                    ih >= 0 && ih < P.I[1];
                 const T* src = xg + (int64_t)ic * in_plane + ((int64_t)id * P.I[1] + ih) * IW;
 #pragma unroll
                 for (int k = 0; k < kGrpStageW; ++k) {
@@ -205,11 +211,13 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                if (r0 + u >= nrows) break;
+                const int rr = r0 + u;
+                if (rr >= nrows) break;
+                const int ic = rr % CIGP, rowi = rr / CIGP;  // rowi = jd * NR + r
 #pragma unroll
                 for (int k = 0; k < kGrpStageW; ++k) {
                     const int iw = lane_s + 32 * k;
-                    if (iw < IW) xs[(r0 + u) * IW + iw] = v[u][k];
+                    if (iw < IW) xs[((int64_t)rowi * IW + iw) * CIGP + ic] = v[u][k];
                 }
             }
         }
@@ -223,7 +231,6 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __
         bv[oc] = (bias != nullptr && oc < P.Cog) ? to_f32(bias[g * P.Cog + oc]) : 0.f;
     const int64_t out_plane = (int64_t)P.O[0] * P.O[1] * P.O[2];
     const int nq = P.qw_ext[0];
-    const int plane_rows = P.Cig * NR * IW;   // floats per D tap in xs
 
     const int rows_per_warp = P.R / kGrpWarps;
     for (int i = 0; i < rows_per_warp; ++i) {
@@ -235,7 +242,7 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __
         T* yrow = y + (b * P.C_out + (int64_t)g * P.Cog) * out_plane +
                   ((int64_t)od * P.O[1] + oh) * P.O[2];
         for (int qb = 0; qb < nq; qb += 64) {
-            const int qv[2] = {qb + lane, qb + 32 + lane};
+            const int qv0 = qb + lane, qv1 = qb + 32 + lane;
             float acc[2][SW][COG];
 #pragma unroll
             for (int u = 0; u < 2; ++u)
@@ -246,29 +253,50 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __
 #pragma unroll
             for (int r = 0; r < SW; ++r) {
                 const int nw_ = P.ntap[2][r];
+                const bool in0 = qv0 < P.qw_ext[r], in1 = qv1 < P.qw_ext[r];
                 for (int jd = 0; jd < nd_; ++jd)
                     for (int jh = 0; jh < nh_; ++jh) {
-                        const int lr = qh + P.off[1][rh][jh] - ih_lo;
-                        const float* xr = xs + jd * plane_rows + lr * IW;
+                        const int lr = jd * NR + qh + P.off[1][rh][jh] - ih_lo;
+                        const float* xr = xs + (int64_t)lr * IW * CIGP;
                         const int tdh = (P.tap[0][rd][jd] * P.Kdims[1] + P.tap[1][rh][jh]) * P.Kdims[2];
                         for (int jw = 0; jw < nw_; ++jw) {
-                            const int ow_off = P.off[2][r][jw];
-                            const float* ws = slab + (tdh + P.tap[2][r][jw]) * P.Cig * COG;
-                            int iw[2];
-                            bool ok[2];
+                            const int o = P.off[2][r][jw];
+                            const int iw0 = qv0 + o, iw1 = qv1 + o;
+                            const bool ok0 = in0 && iw0 >= 0 && iw0 < IW;
+                            const bool ok1 = in1 && iw1 >= 0 && iw1 < IW;
+                            const float4* ws =
+                                reinterpret_cast<const float4*>(slab + (tdh + P.tap[2][r][jw]) * CIGP * COG);
+                            const float4* x0p = reinterpret_cast<const float4*>(xr + (ok0 ? iw0 : 0) * CIGP);
+                            const float4* x1p = reinterpret_cast<const float4*>(xr + (ok1 ? iw1 : 0) * CIGP);
 #pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                iw[u] = qv[u] + ow_off;
-                                ok[u] = qv[u] < P.qw_ext[r] && iw[u] >= 0 && iw[u] < IW;
-                            }
-                            for (int ic = 0; ic < P.Cig; ++ic) {
-                                const float* wv = ws + ic * COG;
-                                const float x0 = ok[0] ? xr[ic * NR * IW + iw[0]] : 0.f;
-                                const float x1 = ok[1] ? xr[ic * NR * IW + iw[1]] : 0.f;
+                            for (int c4 = 0; c4 < CIGP / 4; ++c4) {
+                                float4 a0 = x0p[c4], a1 = x1p[c4];
+                                if (!ok0) a0 = make_float4(0.f, 0.f, 0.f, 0.f);
+                                if (!ok1) a1 = make_float4(0.f, 0.f, 0.f, 0.f);
+                                const float xa[4] = {a0.x, a0.y, a0.z, a0.w};
+                                const float xb[4] = {a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-                                for (int oc = 0; oc < COG; ++oc) {
-                                    acc[0][r][oc] = fmaf(x0, wv[oc], acc[0][r][oc]);
-                                    acc[1][r][oc] = fmaf(x1, wv[oc], acc[1][r][oc]);
+                                for (int ii = 0; ii < 4; ++ii) {
+                                    const int ic = c4 * 4 + ii;
+#pragma unroll
+                                    for (int o4 = 0; o4 < COG / 4 || (COG < 4 && o4 == 0); ++o4) {
+                                        if constexpr (COG >= 4) {
+                                            const float4 wv = ws[(ic * COG) / 4 + o4];
+                                            const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                                            for (int jj = 0; jj < 4; ++jj) {
+                                                acc[0][r][o4 * 4 + jj] = fmaf(xa[ii], wa[jj], acc[0][r][o4 * 4 + jj]);
+                                                acc[1][r][o4 * 4 + jj] = fmaf(xb[ii], wa[jj], acc[1][r][o4 * 4 + jj]);
+                                            }
+                                        } else {
+                                            const float* wsc = reinterpret_cast<const float*>(ws) + ic * COG;
+#pragma unroll
+                                            for (int jj = 0; jj < COG; ++jj) {
+                                                acc[0][r][jj] = fmaf(xa[ii], wsc[jj], acc[0][r][jj]);
+                                                acc[1][r][jj] = fmaf(xb[ii], wsc[jj], acc[1][r][jj]);
+                                            }
+                                        }
+                                    }
                                 }
                             }
                         }
@@ -276,12 +304,19 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __
             }
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                const int q = qv[u];
+                const int q = u ? qv1 : qv0;
                 if (q >= nq) continue;
 #pragma unroll
                 for (int oc = 0; oc < COG; ++oc) {
                     if (oc >= P.Cog) break;
                     T* yo = yrow + (int64_t)oc * out_plane + (int64_t)SW * q;
+                    if constexpr (SW == 2 && sizeof(T) == 4) {
+                        if (P.vec2 && q < P.qw_ext[1]) {
+                            *reinterpret_cast<float2*>(yo) =
+                                make_float2(acc[u][0][oc] + bv[oc], acc[u][1][oc] + bv[oc]);
+                            continue;
+                        }
+                    }
 #pragma unroll
                     for (int r = 0; r < SW; ++r)
                         if (q < P.qw_ext[r]) yo[r] = from_f32<T>(acc[u][r][oc] + bv[oc]);
@@ -295,7 +330,7 @@ struct GroupedPlan {
     AxisPlan ax[3];
     int cog_pad;
     bool staged;
-    int R, nr_max, offmin_h;
+    int R, nr_max, offmin_h, cigp;
     size_t smem;
 };
 
@@ -331,11 +366,13 @@ bool make_plan(const Problem& p, GroupedPlan* pl) {
         }
     for (int r = 0; r < p.S[0]; ++r) ndmax = std::max(ndmax, pl->ax[0].ntaps[r]);
     pl->staged = false;
-    if (offmin <= offmax && p.I[2] <= 32 * kGrpStageW) {
+    pl->cigp = p.Cig <= 4 ? 4 : p.Cig <= 8 ? 8 : p.Cig <= 16 ? 16 : 0;
+    if (offmin <= offmax && p.I[2] <= 32 * kGrpStageW && pl->cigp > 0) {
         for (int R : {16, 8}) {
             // floor((oh0 + R - 1) / s) - floor(oh0 / s) <= floor((R - 1) / s) + 1
             const int nr = (R - 1) / p.S[1] + 2 + (offmax - offmin);
-            const size_t sm = slab + (size_t)std::max(ndmax, 1) * p.Cig * nr * p.I[2] * sizeof(float);
+            const size_t wslab = (size_t)p.taps() * pl->cigp * pl->cog_pad * sizeof(float);
+            const size_t sm = wslab + (size_t)std::max(ndmax, 1) * pl->cigp * nr * p.I[2] * sizeof(float);
             if (sm <= kGrpMaxStaged) {
                 pl->staged = true;
                 pl->R = R;
@@ -349,16 +386,25 @@ bool make_plan(const Problem& p, GroupedPlan* pl) {
     return true;
 }
 
+template <typename T, int SW, int COG, int CIGP>
+cudaError_t launch_staged(const GroupedParams& P, int64_t blocks, size_t smem, cudaStream_t stream) {
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(grouped_staged_kernel<T, SW, COG, CIGP>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    grouped_staged_kernel<T, SW, COG, CIGP><<<(unsigned)blocks, kGrpWarps * 32, smem, stream>>>(P);
+    return cudaGetLastError();
+}
+
 template <typename T, int SW, int COG>
 cudaError_t launch_grouped_t(const GroupedParams& P, int64_t blocks, size_t smem, cudaStream_t stream) {
     if (P.R > 0) {
-        if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(grouped_staged_kernel<T, SW, COG>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)smem);
-            if (e != cudaSuccess) return e;
+        switch (P.cigp) {
+            case 4: return launch_staged<T, SW, COG, 4>(P, blocks, smem, stream);
+            case 8: return launch_staged<T, SW, COG, 8>(P, blocks, smem, stream);
+            default: return launch_staged<T, SW, COG, 16>(P, blocks, smem, stream);
         }
-        grouped_staged_kernel<T, SW, COG><<<(unsigned)blocks, kGrpWarps * 32, smem, stream>>>(P);
     } else {
         grouped_kernel<T, SW, COG><<<(unsigned)blocks, kGrpWarps * 32, smem, stream>>>(P);
     }
@@ -435,6 +481,8 @@ cudaError_t launch_grouped(const Problem& p, const void* x, const void* w, const
         P.n_band = (int)((p.O[1] + pl.R - 1) / pl.R);
         P.nr_max = pl.nr_max;
         P.offmin_h = pl.offmin_h;
+        P.cigp = pl.cigp;
+        P.vec2 = p.dtype == CT_F32 && p.S[2] == 2 && (p.O[2] % 2) == 0 && ((uintptr_t)y % 8) == 0;
         blocks = p.B * (int64_t)p.G * p.O[0] * P.n_band;
         slab = pl.smem;
     }
