@@ -10,7 +10,8 @@
 // that fp32 problems keep fp32 accuracy.  Two kernels run:
 //   1. simt_weight_reorder : w [C_in, C_out, taps] -> W' [taps][C_in_pad][N_pad]
 //   2. simt_phase_gemm     : 128 (oc) x 128 (q) tiles, K in steps of 8,
-//      256 threads with 8 x 8 register tiles, both operands double-buffered
+//      256 threads with 8 x 8 register tiles (packed two-lane fp32 FMAs,
+//      fma.rn.f32x2, the same IEEE result as fmaf), both operands double-buffered
 //      in shared memory through cp.async (weights 16 bytes at a time, the
 //      tap-shifted x window 4 bytes at a time since its start is arbitrary),
 //      bias added in fp32 at the end.
@@ -127,11 +128,12 @@ __global__ void __launch_bounds__(kSimtThreads, 2) simt_phase_gemm(const __grid_
         }
     };
 
-    float acc[8][8];
+    // acc2[i][jj] holds outputs (oc_i, q_{2jj}) and (oc_i, q_{2jj+1})
+    float2 acc2[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+        for (int j = 0; j < 4; ++j) acc2[i][j] = make_float2(0.f, 0.f);
 
     if (nk > 0) {
         load_tile(0, 0);
@@ -153,11 +155,14 @@ __global__ void __launch_bounds__(kSimtThreads, 2) simt_phase_gemm(const __grid_
                 const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][k][tx * 4]);
                 const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][k][tx * 4 + 64]);
                 const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                const float2 bb[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
+                                      make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
+                for (int i = 0; i < 8; ++i) {
+                    const float2 ad = make_float2(a[i], a[i]);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
+                    for (int j = 0; j < 4; ++j) fma2(acc2[i][j], ad, bb[j]);
+                }
             }
             __syncthreads();
         }
@@ -175,7 +180,8 @@ __global__ void __launch_bounds__(kSimtThreads, 2) simt_phase_gemm(const __grid_
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int q = q0 + tx * 4 + (j & 3) + (j >> 2) * 64;
-            if (q < qext) yr[rw + (int64_t)P.S[2] * q] = acc[i][j] + bv;
+            const float a = (j & 1) ? acc2[i][j >> 1].y : acc2[i][j >> 1].x;
+            if (q < qext) yr[rw + (int64_t)P.S[2] * q] = a + bv;
         }
     }
 }
