@@ -51,6 +51,7 @@ struct GroupedParams {
     int R, n_band, nr_max, offmin_h;
     int vec2;              // fp32, stride 2 along W: rows 8-byte aligned (float2 stores)
     int cigp;              // staged variant: channels per group padded to 4, 8 or 16
+    int ws, base_w;        // staged row: WS positions p, iw = p + base_w
 };
 
 // slab layout: [tap][ic][COG] (COG >= Cog, zero padded)
@@ -146,13 +147,15 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_kernel(const __grid_co
 
 
 // Staged variant: one block per (b, g, od, band of R output rows).  The input
-// rows the band reads (every D tap of the depth's phase, the H rows of all the
-// band's rows, the full W extent, the group's channels padded to CIGP) are
-// first copied into shared memory channels-innermost ([row][w][ic], zeros
-// outside the input), so that for one tap a lane reads its CIGP channels with
-// CIGP/4 16-byte loads at fixed offsets.  Each lane owns two q positions of a
-// row (q and q + 32) and every W residue of them; per tap the COG x CIGP
-// weights are loaded once (broadcast) and used for both positions.
+// rows the band reads (every D tap of the depth's phase and the H rows of all
+// the band's rows) are first copied into shared memory channels-innermost,
+// [row][p][ic] with CIGP channels (zero padded) and WS positions p covering
+// iw = p + base_w for every position slot and tap offset (zeros outside the
+// input), so the tap loop needs no bounds checks: for one tap a lane reads
+// its CIGP channels with CIGP/4 16-byte loads.  Each lane owns two q
+// positions of a row (q and q + 32) and every W residue of them; per tap and
+// channel the COG weights are loaded once (broadcast) and used for both
+// positions with packed two-lane fp32 FMAs over output-channel pairs.
 template <typename T, int SW, int COG, int CIGP>
 __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __grid_constant__ GroupedParams P) {
     extern __shared__ __align__(16) float sm[];
@@ -160,6 +163,7 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __
     const T* __restrict__ w = static_cast<const T*>(P.w);
     const T* __restrict__ bias = static_cast<const T*>(P.bias);
     T* __restrict__ y = static_cast<T*>(P.y);
+    constexpr int COGP = COG < 2 ? 2 : COG;   // padded to an even count for f32x2 pairs
 
     int64_t blk = blockIdx.x;
     const int band = (int)(blk % P.n_band); blk /= P.n_band;
@@ -171,63 +175,52 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __
     const int oh0 = band * P.R;
     const int ih_lo = oh0 / P.S[1] + P.offmin_h;
     const int NR = P.nr_max;
-    const int IW = P.I[2];
+    const int WS = P.ws;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    // weights: slab[tap][ic][oc], CIGP x COG per tap (zero padded)
+    // weights: slab[tap][ic][oc], CIGP x COGP per tap (zero padded)
     float* slab = sm;
-    float* xs = sm + P.taps * CIGP * COG;  // [jd][r][iw][CIGP]
-    const int slab_n = P.taps * CIGP * COG;
+    float* xs = sm + P.taps * CIGP * COGP;  // [jd * NR + r][p][CIGP]
+    const int slab_n = P.taps * CIGP * COGP;
     for (int e = threadIdx.x; e < slab_n; e += blockDim.x) {
-        const int oc = e % COG;
-        const int ic = (e / COG) % CIGP;
-        const int t = e / (COG * CIGP);
+        const int oc = e % COGP;
+        const int ic = (e / COGP) % CIGP;
+        const int t = e / (COGP * CIGP);
         float v = 0.f;
         if (oc < P.Cog && ic < P.Cig)
             v = to_f32(w[((int64_t)(g * P.Cig + ic) * P.Cog + oc) * P.taps + t]);
         slab[e] = v;
     }
-    const int64_t in_plane = (int64_t)P.I[0] * P.I[1] * IW;
+    const int64_t in_plane = (int64_t)P.I[0] * P.I[1] * P.I[2];
     const T* xg = x + (b * P.C_in + (int64_t)g * P.Cig) * in_plane;
-    {
-        // one (jd, r, ic) input row per warp iteration, lanes along W
-        const int warp_s = threadIdx.x / 32, lane_s = threadIdx.x % 32;
-        const int nrows = nd_ * NR * CIGP;
-        for (int r0 = warp_s * 4; r0 < nrows; r0 += kGrpWarps * 4) {
-            float v[4][kGrpStageW];
+    // one staged row (jd, r) per warp iteration: all CIGP channels, lanes on p
+    for (int rowi = warp; rowi < nd_ * NR; rowi += kGrpWarps) {
+        const int jd = rowi / NR, r = rowi - jd * NR;
+        const int id = qd + P.off[0][rd][jd];
+        const int ih = ih_lo + r;
+        const bool row_ok = id >= 0 && id < P.I[0] && ih >= 0 && ih < P.I[1];
+        const T* src = xg + ((int64_t)id * P.I[1] + ih) * P.I[2];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int rr = r0 + u;
-                const int ic = rr % CIGP, r = (rr / CIGP) % NR, jd = rr / (CIGP * NR);
-                const int id = rr < nrows ? qd + P.off[0][rd][jd] : -1;
-                const int ih = ih_lo + r;
-                const bool row_ok = rr < nrows && ic < P.Cig && id >= 0 && id < P.I[0] &&
-                                    ih >= 0 && ih < P.I[1];
-                const T* src = xg + (int64_t)ic * in_plane + ((int64_t)id * P.I[1] + ih) * IW;
+        for (int k = 0; k < kGrpStageW; ++k) {
+            const int pp = lane + 32 * k;
+            if (pp >= WS) break;
+            const int iw = pp + P.base_w;
+            const bool ok = row_ok && iw >= 0 && iw < P.I[2];
+            float v[CIGP];
 #pragma unroll
-                for (int k = 0; k < kGrpStageW; ++k) {
-                    const int iw = lane_s + 32 * k;
-                    v[u][k] = (row_ok && iw < IW) ? to_f32(src[iw]) : 0.f;
-                }
-            }
+            for (int ic = 0; ic < CIGP; ++ic)
+                v[ic] = (ok && ic < P.Cig) ? to_f32(src[(int64_t)ic * in_plane + iw]) : 0.f;
+            float4* dst = reinterpret_cast<float4*>(xs + ((int64_t)rowi * WS + pp) * CIGP);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int rr = r0 + u;
-                if (rr >= nrows) break;
-                const int ic = rr % CIGP, rowi = rr / CIGP;  // rowi = jd * NR + r
-#pragma unroll
-                for (int k = 0; k < kGrpStageW; ++k) {
-                    const int iw = lane_s + 32 * k;
-                    if (iw < IW) xs[((int64_t)rowi * IW + iw) * CIGP + ic] = v[u][k];
-                }
-            }
+            for (int c4 = 0; c4 < CIGP / 4; ++c4)
+                dst[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
         }
     }
     __syncthreads();
 
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    float bv[COG];
+    float bv[COGP];
 #pragma unroll
-    for (int oc = 0; oc < COG; ++oc)
+    for (int oc = 0; oc < COGP; ++oc)
         bv[oc] = (bias != nullptr && oc < P.Cog) ? to_f32(bias[g * P.Cog + oc]) : 0.f;
     const int64_t out_plane = (int64_t)P.O[0] * P.O[1] * P.O[2];
     const int nq = P.qw_ext[0];
@@ -243,59 +236,40 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __
                   ((int64_t)od * P.O[1] + oh) * P.O[2];
         for (int qb = 0; qb < nq; qb += 64) {
             const int qv0 = qb + lane, qv1 = qb + 32 + lane;
-            float acc[2][SW][COG];
+            float2 acc[2][SW][COGP / 2];
 #pragma unroll
             for (int u = 0; u < 2; ++u)
 #pragma unroll
                 for (int r = 0; r < SW; ++r)
 #pragma unroll
-                    for (int oc = 0; oc < COG; ++oc) acc[u][r][oc] = 0.f;
+                    for (int o2 = 0; o2 < COGP / 2; ++o2) acc[u][r][o2] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int r = 0; r < SW; ++r) {
                 const int nw_ = P.ntap[2][r];
-                const bool in0 = qv0 < P.qw_ext[r], in1 = qv1 < P.qw_ext[r];
                 for (int jd = 0; jd < nd_; ++jd)
                     for (int jh = 0; jh < nh_; ++jh) {
                         const int lr = jd * NR + qh + P.off[1][rh][jh] - ih_lo;
-                        const float* xr = xs + (int64_t)lr * IW * CIGP;
+                        const float* xr = xs + ((int64_t)lr * WS + qv0 - P.base_w) * CIGP;
                         const int tdh = (P.tap[0][rd][jd] * P.Kdims[1] + P.tap[1][rh][jh]) * P.Kdims[2];
                         for (int jw = 0; jw < nw_; ++jw) {
-                            const int o = P.off[2][r][jw];
-                            const int iw0 = qv0 + o, iw1 = qv1 + o;
-                            const bool ok0 = in0 && iw0 >= 0 && iw0 < IW;
-                            const bool ok1 = in1 && iw1 >= 0 && iw1 < IW;
-                            const float4* ws =
-                                reinterpret_cast<const float4*>(slab + (tdh + P.tap[2][r][jw]) * CIGP * COG);
-                            const float4* x0p = reinterpret_cast<const float4*>(xr + (ok0 ? iw0 : 0) * CIGP);
-                            const float4* x1p = reinterpret_cast<const float4*>(xr + (ok1 ? iw1 : 0) * CIGP);
+                            const float4* x0p = reinterpret_cast<const float4*>(xr + P.off[2][r][jw] * CIGP);
+                            const float4* x1p = x0p + 32 * CIGP / 4;
+                            const float* ws = slab + (tdh + P.tap[2][r][jw]) * CIGP * COGP;
 #pragma unroll
                             for (int c4 = 0; c4 < CIGP / 4; ++c4) {
-                                float4 a0 = x0p[c4], a1 = x1p[c4];
-                                if (!ok0) a0 = make_float4(0.f, 0.f, 0.f, 0.f);
-                                if (!ok1) a1 = make_float4(0.f, 0.f, 0.f, 0.f);
+                                const float4 a0 = x0p[c4], a1 = x1p[c4];
                                 const float xa[4] = {a0.x, a0.y, a0.z, a0.w};
                                 const float xb[4] = {a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
                                 for (int ii = 0; ii < 4; ++ii) {
-                                    const int ic = c4 * 4 + ii;
+                                    const float* wr = ws + (c4 * 4 + ii) * COGP;
+                                    const float2 d0 = make_float2(xa[ii], xa[ii]);
+                                    const float2 d1 = make_float2(xb[ii], xb[ii]);
 #pragma unroll
-                                    for (int o4 = 0; o4 < COG / 4 || (COG < 4 && o4 == 0); ++o4) {
-                                        if constexpr (COG >= 4) {
-                                            const float4 wv = ws[(ic * COG) / 4 + o4];
-                                            const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                                            for (int jj = 0; jj < 4; ++jj) {
-                                                acc[0][r][o4 * 4 + jj] = fmaf(xa[ii], wa[jj], acc[0][r][o4 * 4 + jj]);
-                                                acc[1][r][o4 * 4 + jj] = fmaf(xb[ii], wa[jj], acc[1][r][o4 * 4 + jj]);
-                                            }
-                                        } else {
-                                            const float* wsc = reinterpret_cast<const float*>(ws) + ic * COG;
-#pragma unroll
-                                            for (int jj = 0; jj < COG; ++jj) {
-                                                acc[0][r][jj] = fmaf(xa[ii], wsc[jj], acc[0][r][jj]);
-                                                acc[1][r][jj] = fmaf(xb[ii], wsc[jj], acc[1][r][jj]);
-                                            }
-                                        }
+                                    for (int o2 = 0; o2 < COGP / 2; ++o2) {
+                                        const float2 wv = *reinterpret_cast<const float2*>(wr + 2 * o2);
+                                        fma2(acc[0][r][o2], d0, wv);
+                                        fma2(acc[1][r][o2], d1, wv);
                                     }
                                 }
                             }
@@ -310,16 +284,20 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __
                 for (int oc = 0; oc < COG; ++oc) {
                     if (oc >= P.Cog) break;
                     T* yo = yrow + (int64_t)oc * out_plane + (int64_t)SW * q;
+                    const float bo = bv[oc];
                     if constexpr (SW == 2 && sizeof(T) == 4) {
                         if (P.vec2 && q < P.qw_ext[1]) {
-                            *reinterpret_cast<float2*>(yo) =
-                                make_float2(acc[u][0][oc] + bv[oc], acc[u][1][oc] + bv[oc]);
+                            const float v0 = (oc & 1) ? acc[u][0][oc >> 1].y : acc[u][0][oc >> 1].x;
+                            const float v1 = (oc & 1) ? acc[u][1][oc >> 1].y : acc[u][1][oc >> 1].x;
+                            *reinterpret_cast<float2*>(yo) = make_float2(v0 + bo, v1 + bo);
                             continue;
                         }
                     }
 #pragma unroll
-                    for (int r = 0; r < SW; ++r)
-                        if (q < P.qw_ext[r]) yo[r] = from_f32<T>(acc[u][r][oc] + bv[oc]);
+                    for (int r = 0; r < SW; ++r) {
+                        const float v = (oc & 1) ? acc[u][r][oc >> 1].y : acc[u][r][oc >> 1].x;
+                        if (q < P.qw_ext[r]) yo[r] = from_f32<T>(v + bo);
+                    }
                 }
             }
         }
@@ -330,7 +308,7 @@ struct GroupedPlan {
     AxisPlan ax[3];
     int cog_pad;
     bool staged;
-    int R, nr_max, offmin_h, cigp;
+    int R, nr_max, offmin_h, cigp, ws, base_w;
     size_t smem;
 };
 
@@ -367,12 +345,25 @@ bool make_plan(const Problem& p, GroupedPlan* pl) {
     for (int r = 0; r < p.S[0]; ++r) ndmax = std::max(ndmax, pl->ax[0].ntaps[r]);
     pl->staged = false;
     pl->cigp = p.Cig <= 4 ? 4 : p.Cig <= 8 ? 8 : p.Cig <= 16 ? 16 : 0;
-    if (offmin <= offmax && p.I[2] <= 32 * kGrpStageW && pl->cigp > 0) {
+    // W span of the staged rows: position slots q in [0, 64 * ceil(nq / 64))
+    // read iw = q + off for every W offset off of every residue
+    int wmin = 1 << 30, wmax = -(1 << 30);
+    for (int r = 0; r < p.S[2]; ++r)
+        for (int j = 0; j < pl->ax[2].ntaps[r]; ++j) {
+            wmin = std::min(wmin, pl->ax[2].off[r][j]);
+            wmax = std::max(wmax, pl->ax[2].off[r][j]);
+        }
+    const int64_t nq_slots = (pl->ax[2].q_extent[0] + 63) / 64 * 64;
+    if (offmin <= offmax && wmin <= wmax && pl->cigp > 0 &&
+        nq_slots + (wmax - wmin) <= 32 * kGrpStageW) {
+        pl->ws = (int)(nq_slots + (wmax - wmin));
+        pl->base_w = wmin;
         for (int R : {16, 8}) {
             // floor((oh0 + R - 1) / s) - floor(oh0 / s) <= floor((R - 1) / s) + 1
             const int nr = (R - 1) / p.S[1] + 2 + (offmax - offmin);
-            const size_t wslab = (size_t)p.taps() * pl->cigp * pl->cog_pad * sizeof(float);
-            const size_t sm = wslab + (size_t)std::max(ndmax, 1) * pl->cigp * nr * p.I[2] * sizeof(float);
+            const int cogp = pl->cog_pad < 2 ? 2 : pl->cog_pad;
+            const size_t wslab = (size_t)p.taps() * pl->cigp * cogp * sizeof(float);
+            const size_t sm = wslab + (size_t)std::max(ndmax, 1) * nr * pl->ws * pl->cigp * sizeof(float);
             if (sm <= kGrpMaxStaged) {
                 pl->staged = true;
                 pl->R = R;
@@ -482,6 +473,8 @@ cudaError_t launch_grouped(const Problem& p, const void* x, const void* w, const
         P.nr_max = pl.nr_max;
         P.offmin_h = pl.offmin_h;
         P.cigp = pl.cigp;
+        P.ws = pl.ws;
+        P.base_w = pl.base_w;
         P.vec2 = p.dtype == CT_F32 && p.S[2] == 2 && (p.O[2] % 2) == 0 && ((uintptr_t)y % 8) == 0;
         blocks = p.B * (int64_t)p.G * p.O[0] * P.n_band;
         slab = pl.smem;
