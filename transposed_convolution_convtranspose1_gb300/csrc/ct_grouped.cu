@@ -34,6 +34,11 @@ constexpr int kGrpWarps = 8;      // rows per block
 constexpr size_t kGrpMaxSlab = 48 * 1024;
 constexpr int kGrpStageW = 4;     // staged variant: input width <= 32 * kGrpStageW
 
+// Floats per staged position: CIGP channels, padded so that lanes reading
+// consecutive positions with 16-byte loads hit distinct bank groups.
+template <int CIGP>
+constexpr int xstride() { return CIGP == 4 ? 4 : CIGP + 4; }
+
 struct GroupedParams {
     const void* x;
     const void* w;
@@ -149,7 +154,8 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_kernel(const __grid_co
 // Staged variant: one block per (b, g, od, band of R output rows).  The input
 // rows the band reads (every D tap of the depth's phase and the H rows of all
 // the band's rows) are first copied into shared memory channels-innermost,
-// [row][p][ic] with CIGP channels (zero padded) and WS positions p covering
+// [row][p][ic] with CIGP channels (zero padded, positions xstride<CIGP>()
+// floats apart) and WS positions p covering
 // iw = p + base_w for every position slot and tap offset (zeros outside the
 // input), so the tap loop needs no bounds checks: for one tap a lane reads
 // its CIGP channels with CIGP/4 16-byte loads.  Each lane owns two q
@@ -210,7 +216,7 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __
 #pragma unroll
             for (int ic = 0; ic < CIGP; ++ic)
                 v[ic] = (ok && ic < P.Cig) ? to_f32(src[(int64_t)ic * in_plane + iw]) : 0.f;
-            float4* dst = reinterpret_cast<float4*>(xs + ((int64_t)rowi * WS + pp) * CIGP);
+            float4* dst = reinterpret_cast<float4*>(xs + ((int64_t)rowi * WS + pp) * xstride<CIGP>());
 #pragma unroll
             for (int c4 = 0; c4 < CIGP / 4; ++c4)
                 dst[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
@@ -249,11 +255,12 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __
                 for (int jd = 0; jd < nd_; ++jd)
                     for (int jh = 0; jh < nh_; ++jh) {
                         const int lr = jd * NR + qh + P.off[1][rh][jh] - ih_lo;
-                        const float* xr = xs + ((int64_t)lr * WS + qv0 - P.base_w) * CIGP;
+                        const float* xr = xs + ((int64_t)lr * WS + qv0 - P.base_w) * xstride<CIGP>();
                         const int tdh = (P.tap[0][rd][jd] * P.Kdims[1] + P.tap[1][rh][jh]) * P.Kdims[2];
                         for (int jw = 0; jw < nw_; ++jw) {
-                            const float4* x0p = reinterpret_cast<const float4*>(xr + P.off[2][r][jw] * CIGP);
-                            const float4* x1p = x0p + 32 * CIGP / 4;
+                            const float4* x0p =
+                                reinterpret_cast<const float4*>(xr + P.off[2][r][jw] * xstride<CIGP>());
+                            const float4* x1p = x0p + 32 * xstride<CIGP>() / 4;
                             const float* ws = slab + (tdh + P.tap[2][r][jw]) * CIGP * COGP;
 #pragma unroll
                             for (int c4 = 0; c4 < CIGP / 4; ++c4) {
@@ -265,11 +272,24 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __
                                     const float* wr = ws + (c4 * 4 + ii) * COGP;
                                     const float2 d0 = make_float2(xa[ii], xa[ii]);
                                     const float2 d1 = make_float2(xb[ii], xb[ii]);
+                                    if constexpr (COGP % 4 == 0) {
 #pragma unroll
-                                    for (int o2 = 0; o2 < COGP / 2; ++o2) {
-                                        const float2 wv = *reinterpret_cast<const float2*>(wr + 2 * o2);
-                                        fma2(acc[0][r][o2], d0, wv);
-                                        fma2(acc[1][r][o2], d1, wv);
+                                        for (int o4 = 0; o4 < COGP / 4; ++o4) {
+                                            const float4 wq = *reinterpret_cast<const float4*>(wr + 4 * o4);
+                                            const float2 wlo = make_float2(wq.x, wq.y);
+                                            const float2 whi = make_float2(wq.z, wq.w);
+                                            fma2(acc[0][r][2 * o4], d0, wlo);
+                                            fma2(acc[1][r][2 * o4], d1, wlo);
+                                            fma2(acc[0][r][2 * o4 + 1], d0, whi);
+                                            fma2(acc[1][r][2 * o4 + 1], d1, whi);
+                                        }
+                                    } else {
+#pragma unroll
+                                        for (int o2 = 0; o2 < COGP / 2; ++o2) {
+                                            const float2 wv = *reinterpret_cast<const float2*>(wr + 2 * o2);
+                                            fma2(acc[0][r][o2], d0, wv);
+                                            fma2(acc[1][r][o2], d1, wv);
+                                        }
                                     }
                                 }
                             }
@@ -363,7 +383,8 @@ bool make_plan(const Problem& p, GroupedPlan* pl) {
             const int nr = (R - 1) / p.S[1] + 2 + (offmax - offmin);
             const int cogp = pl->cog_pad < 2 ? 2 : pl->cog_pad;
             const size_t wslab = (size_t)p.taps() * pl->cigp * cogp * sizeof(float);
-            const size_t sm = wslab + (size_t)std::max(ndmax, 1) * nr * pl->ws * pl->cigp * sizeof(float);
+            const int xst = pl->cigp == 4 ? 4 : pl->cigp + 4;  // xstride<CIGP>()
+            const size_t sm = wslab + (size_t)std::max(ndmax, 1) * nr * pl->ws * xst * sizeof(float);
             if (sm <= kGrpMaxStaged) {
                 pl->staged = true;
                 pl->R = R;
