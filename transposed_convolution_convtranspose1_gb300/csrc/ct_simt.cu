@@ -9,11 +9,12 @@
 // conv-transpose2d-phase-gemm-tiled) -- computed here in exact fp32 FMA so
 // that fp32 problems keep fp32 accuracy.  Two kernels run:
 //   1. simt_weight_reorder : w [C_in, C_out, taps] -> W' [taps][C_in_pad][N_pad]
-//   2. simt_phase_gemm     : 128 (oc) x 128 (q) tiles, K in steps of 8,
+//   2. simt_phase_gemm     : 128 (oc) x 128 (q) tiles, K in steps of 16,
 //      256 threads with 8 x 8 register tiles (packed two-lane fp32 FMAs,
-//      fma.rn.f32x2, the same IEEE result as fmaf), both operands double-buffered
-//      in shared memory through cp.async (weights 16 bytes at a time, the
-//      tap-shifted x window 4 bytes at a time since its start is arbitrary),
+//      fma.rn.f32x2, the same IEEE result as fmaf), both operands staged
+//      in a three-stage shared-memory ring through cp.async (weights 16 bytes
+//      at a time, the tap-shifted x window 4 bytes at a time since its start
+//      is arbitrary, lanes on consecutive elements), one barrier per k-tile,
 //      bias added in fp32 at the end.
 #include <algorithm>
 #include <cstring>
@@ -26,7 +27,8 @@ namespace {
 
 constexpr int kBM = 128;  // output channels per tile
 constexpr int kBN = 128;  // q positions per tile
-constexpr int kBK = 8;    // reduction step
+constexpr int kBK = 16;   // reduction step
+constexpr int kStages = 3; // cp.async pipeline depth
 constexpr int kSimtThreads = 256;
 constexpr int kSimtMaxS = 8;
 constexpr int kSimtMaxTaps = 16;
@@ -69,8 +71,10 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 __global__ void __launch_bounds__(kSimtThreads, 2) simt_phase_gemm(const __grid_constant__ SimtParams P) {
-    __shared__ __align__(16) float As[2][kBK][kBM];
-    __shared__ __align__(16) float Bs[2][kBK][kBN];
+    extern __shared__ __align__(16) float smem_f[];
+    // stage s: As[s][k][oc] then Bs[s][k][q]
+    auto As = [&](int s, int k) { return smem_f + (size_t)s * 2 * kBK * kBM + (size_t)k * kBM; };
+    auto Bs = [&](int s, int k) { return smem_f + (size_t)s * 2 * kBK * kBM + (size_t)(kBK + k) * kBN; };
 
     // block -> (oc block, q block, W residue, output row (b, od, oh))
     int64_t blk = blockIdx.x;
@@ -88,6 +92,7 @@ __global__ void __launch_bounds__(kSimtThreads, 2) simt_phase_gemm(const __grid_
 
     const int tid = threadIdx.x;
     const int tx = tid % 16, ty = tid / 16;
+    const int warp = tid / 32, lane = tid % 32;
 
     const int nd_ = P.ntap[0][rd], nh_ = P.ntap[1][rh], nw_ = P.ntap[2][rw];
     const int ntaps = nd_ * nh_ * nw_;
@@ -97,34 +102,34 @@ __global__ void __launch_bounds__(kSimtThreads, 2) simt_phase_gemm(const __grid_
     const int64_t in_plane = (int64_t)P.I[0] * P.I[1] * P.I[2];
     const float* xb = P.x + b * P.C_in * in_plane;
 
-    // loader assignment: A tile 8 x 128 floats = 256 x float4; B tile 8 x 128
-    // floats = 256 threads x 4 floats
-    const int a_k = tid / 32, a_c = (tid % 32) * 4;
-    const int b_k = tid / 32, b_c = (tid % 32) * 4;
-
-    auto load_tile = [&](int kt, int buf) {
+    // A tile: 16 x 128 floats = 512 float4, two per thread (rows warp, warp + 8);
+    // B tile: 16 x 128 floats, rows warp and warp + 8, lanes on consecutive floats
+    auto load_tile = [&](int kt, int st) {
         const int j = kt / kchunks;
         const int ic0 = (kt % kchunks) * kBK;
         const int jw = j % nw_;
         const int jh = (j / nw_) % nh_;
         const int jd = j / (nw_ * nh_);
-        const int td = P.tap[0][rd][jd], th = P.tap[1][rh][jh], tw = P.tap[2][rw][jw];
-        const int tap = (td * P.Kdims[1] + th) * P.Kdims[2] + tw;
-        // weights: row (tap, ic0 + a_k), channels oc0 + a_c .. +3
-        cp_async16(&As[buf][a_k][a_c],
-                   P.wp + ((int64_t)tap * P.C_in_pad + ic0 + a_k) * P.N_pad + oc0 + a_c);
-        // x window: channel ic0 + b_k, row (id, ih), positions q0 + b_c + i + off_w
-        const int ic = ic0 + b_k;
+        const int tap = (P.tap[0][rd][jd] * P.Kdims[1] + P.tap[1][rh][jh]) * P.Kdims[2] + P.tap[2][rw][jw];
         const int id = qd + P.off[0][rd][jd];
         const int ih = qh + P.off[1][rh][jh];
-        const int iw0 = q0 + b_c + P.off[2][rw][jw];
-        const bool row_ok = ic < P.C_in && id >= 0 && id < P.I[0] && ih >= 0 && ih < P.I[1];
-        const float* xr = xb + (int64_t)ic * in_plane + ((int64_t)id * P.I[1] + ih) * P.I[2];
+        const int iwb = q0 + P.off[2][rw][jw];
+        const bool dh_ok = id >= 0 && id < P.I[0] && ih >= 0 && ih < P.I[1];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int iw = iw0 + i;
-            const bool ok = row_ok && iw >= 0 && iw < P.I[2];
-            cp_async4(&Bs[buf][b_k][b_c + i], ok ? xr + iw : P.x, ok);
+        for (int h = 0; h < 2; ++h) {
+            const int k = warp + 8 * h;
+            cp_async16(As(st, k) + lane * 4,
+                       P.wp + ((int64_t)tap * P.C_in_pad + ic0 + k) * P.N_pad + oc0 + lane * 4);
+            const int ic = ic0 + k;
+            const bool row_ok = dh_ok && ic < P.C_in;
+            const float* xr = xb + (int64_t)ic * in_plane + ((int64_t)id * P.I[1] + ih) * P.I[2];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int col = lane + 32 * i;
+                const int iw = iwb + col;
+                const bool ok = row_ok && iw >= 0 && iw < P.I[2];
+                cp_async4(Bs(st, k) + col, ok ? xr + iw : P.x, ok);
+            }
         }
     };
 
@@ -136,24 +141,27 @@ __global__ void __launch_bounds__(kSimtThreads, 2) simt_phase_gemm(const __grid_
         for (int j = 0; j < 4; ++j) acc2[i][j] = make_float2(0.f, 0.f);
 
     if (nk > 0) {
-        load_tile(0, 0);
-        cp_async_commit();
+        // prologue: stages 0 .. kStages-2
+#pragma unroll
+        for (int st = 0; st < kStages - 1; ++st) {
+            if (st < nk) load_tile(st, st);
+            cp_async_commit();
+        }
         for (int kt = 0; kt < nk; ++kt) {
-            const int buf = kt & 1;
-            if (kt + 1 < nk) {
-                load_tile(kt + 1, buf ^ 1);
+            cp_async_wait<kStages - 2>();  // tile kt has landed
+            __syncthreads();               // and every thread is done with tile kt - 1
+            {
+                const int kn = kt + kStages - 1;
+                if (kn < nk) load_tile(kn, kn % kStages);
                 cp_async_commit();
-                cp_async_wait<1>();
-            } else {
-                cp_async_wait<0>();
             }
-            __syncthreads();
+            const int st = kt % kStages;
 #pragma unroll
             for (int k = 0; k < kBK; ++k) {
-                const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][k][ty * 4]);
-                const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][k][ty * 4 + 64]);
-                const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][k][tx * 4]);
-                const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][k][tx * 4 + 64]);
+                const float4 a0 = *reinterpret_cast<const float4*>(As(st, k) + ty * 4);
+                const float4 a1 = *reinterpret_cast<const float4*>(As(st, k) + ty * 4 + 64);
+                const float4 b0 = *reinterpret_cast<const float4*>(Bs(st, k) + tx * 4);
+                const float4 b1 = *reinterpret_cast<const float4*>(Bs(st, k) + tx * 4 + 64);
                 const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
                 const float2 bb[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
                                       make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
@@ -164,8 +172,8 @@ __global__ void __launch_bounds__(kSimtThreads, 2) simt_phase_gemm(const __grid_
                     for (int j = 0; j < 4; ++j) fma2(acc2[i][j], ad, bb[j]);
                 }
             }
-            __syncthreads();
         }
+        cp_async_wait<0>();
     }
 
     // epilogue: y[b, oc, od, oh, ow = rw + s_w * q] = acc + bias[oc]
@@ -282,8 +290,11 @@ cudaError_t launch_simt(const Problem& p, const void* x, const void* w, const vo
         p.B * p.O[0] * p.O[1] * (int64_t)p.S[2] * P.n_qblk * (int64_t)P.n_ocblk;
     if (blocks >= (1ll << 31)) return cudaErrorInvalidConfiguration;
     P.n_blocks = blocks;
+    const size_t smem = (size_t)kStages * 2 * kBK * kBM * sizeof(float);
+    e = cudaFuncSetAttribute(simt_phase_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     prof_begin(prof, stream);
-    simt_phase_gemm<<<(unsigned)blocks, kSimtThreads, 0, stream>>>(P);
+    simt_phase_gemm<<<(unsigned)blocks, kSimtThreads, smem, stream>>>(P);
     prof_end(prof, stream);
     prof_count(prof);
     return cudaGetLastError();
