@@ -100,7 +100,7 @@ def load_peaks():
 # the source file its DRAM traffic figure depends on.
 ROUTE_KERNEL = {
     "gather": ("gather_kernel", "alu", "ct_gather.cu"),
-    "grouped": ("grouped_kernel", "hbm", "ct_grouped.cu"),
+    "grouped": ("grouped_staged_kernel", "hbm", "ct_grouped.cu"),
     "simt_gemm": ("simt_phase_gemm", "alu", "ct_simt.cu"),
     "tc_gemm": ("tc_phase_gemm", "tensor", "ct_tc.cu"),
     "bias_fill": ("bias_fill_kernel", "hbm", "ct_gather.cu"),
