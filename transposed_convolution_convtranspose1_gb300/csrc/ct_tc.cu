@@ -327,6 +327,18 @@ __device__ __forceinline__ bool tile_has_work(const TcParams& P, const Tile& T) 
     return false;
 }
 
+// W residue processed at step k of a tile.  For SW = 2 the phase with more
+// taps goes first, so that its MMAs (the longer window) overlap the previous
+// tile's final epilogue; otherwise phases run in residue order.
+template <int SW>
+__device__ __forceinline__ int phase_of(const TcParams& P, const Tile& T, int k) {
+    if constexpr (SW == 2) {
+        const bool swap = phase_taps<SW>(P, T, 1) > phase_taps<SW>(P, T, 0);
+        return swap ? 1 - k : k;
+    }
+    return k;
+}
+
 // Tile shape as a function of the W stride SW.
 template <int SW>
 struct TcShape {
@@ -408,7 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
         bool ok = true;
         for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
             const Tile tl = decode_tile(P, t);
-            for (int rw = 0; rw < SW && ok; ++rw) {
+            for (int step = 0; step < SW && ok; ++step) {
+                const int rw = phase_of<SW>(P, tl, step);
                 const int nd_ = P.ntap[0][tl.rd], nh_ = P.ntap[1][tl.rh], nw_ = P.ntap[2][rw];
                 for (int jd = 0; jd < nd_ && ok; ++jd)
                     for (int jh = 0; jh < nh_ && ok; ++jh)
@@ -459,8 +472,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
             for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
                 const Tile tl = decode_tile(P, t);
                 if (!tile_has_work<SW>(P, tl)) continue;
-                for (int rw = 0; rw < SW && ok; ++rw) {
-                    const int slot = SW == 1 ? (int)(work_iter & 1) : rw;
+                for (int step = 0; step < SW && ok; ++step) {
+                    const int rw = phase_of<SW>(P, tl, step);
+                    const int slot = SW == 1 ? (int)(work_iter & 1) : step;
                     const uint32_t use = SW == 1 ? (work_iter >> 1) : work_iter;
                     if (!mbar_wait(smem_u32(&sempty_bar[slot]), (use & 1) ^ 1, kErrMma,
                                    &abort_flag)) {
@@ -531,12 +545,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
             };
 
             uint32_t held[SW > 1 ? SW - 1 : 1][Sh::NPW / 2];  // packed 16-bit outputs
-            // phases 0 .. SW-2 (SW >= 2): convert and hold, release the slot
+            // steps 0 .. SW-2 (SW >= 2): convert the step's phase, hold it, release
+            // its slot (slot = step)
 #pragma unroll
-            for (int rw = 0; rw < SW - 1; ++rw) {
+            for (int st = 0; st < SW - 1; ++st) {
+                const int rw = phase_of<SW>(P, Tl, st);
                 const bool has = work && phase_taps<SW>(P, Tl, rw) > 0;
                 if (work) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sfull_bar[rw]), work_iter & 1,
+                    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sfull_bar[st]), work_iter & 1,
                                                            kErrEpilogue, &abort_flag));
                     if (!ok) break;
                     tc_fence_after();
@@ -546,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                     int oh, qwb;
                     float v[Sh::CQ];
                     if (has && chunk_valid(c, oh, qwb)) {
-                        tmem_ld32(lane_addr + (uint32_t)(rw * Sh::NP + base + c * Sh::CQ), v);
+                        tmem_ld32(lane_addr + (uint32_t)(st * Sh::NP + base + c * Sh::CQ), v);
                         tmem_ld_wait();
                     } else {
 #pragma unroll
@@ -554,19 +570,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                     }
 #pragma unroll
                     for (int i = 0; i < Sh::CQ / 2; ++i)
-                        held[rw][c * (Sh::CQ / 2) + i] = bits16(from_f32<T>(v[2 * i] + bv)) |
+                        held[st][c * (Sh::CQ / 2) + i] = bits16(from_f32<T>(v[2 * i] + bv)) |
                                                          (bits16(from_f32<T>(v[2 * i + 1] + bv)) << 16);
                 }
                 if (work) {
                     tc_fence_before();
-                    mbar_arrive(smem_u32(&sempty_bar[rw]));
+                    mbar_arrive(smem_u32(&sempty_bar[st]));
                 }
             }
             if (!ok) break;
             // last phase (all of it for SW = 1): combine and store
             {
-                const int rl = SW - 1;
-                const int slot = SW == 1 ? (int)(work_iter & 1) : rl;
+                const int rl = phase_of<SW>(P, Tl, SW - 1);  // W residue of the last step
+                const int slot = SW == 1 ? (int)(work_iter & 1) : SW - 1;
                 const uint32_t use = SW == 1 ? (work_iter >> 1) : work_iter;
                 const bool has = work && phase_taps<SW>(P, Tl, rl) > 0;
                 if (work) {
@@ -603,8 +619,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                                 for (int hh = 0; hh < 4; ++hh) {
                                     const int qi = pc * 4 + hh;  // outputs 2qi (phase 0), 2qi+1
                                     const uint32_t w2 = held[0][c * (Sh::CQ / 2) + qi / 2];
-                                    const uint32_t lo = (qi & 1) ? (w2 >> 16) : (w2 & 0xFFFFu);
-                                    wv[hh] = lo | (bits16(from_f32<T>(v[qi] + bv)) << 16);
+                                    const uint32_t h16 = (qi & 1) ? (w2 >> 16) : (w2 & 0xFFFFu);
+                                    const uint32_t v16 = bits16(from_f32<T>(v[qi] + bv));
+                                    wv[hh] = rl == 1 ? (h16 | (v16 << 16)) : (v16 | (h16 << 16));
                                 }
                                 const uint32_t a = sbuf + lane * 128 + ((pc ^ (lane & 7)) << 4);
                                 asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
@@ -631,10 +648,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                             for (int e = 0; e < 2; ++e) {
                                 const int j = pc * 8 + hh * 2 + e;
                                 const int qi = j / SW, r = j % SW;
-                                if (r == SW - 1) {
+                                if (r == rl) {
                                     two[e] = bits16(from_f32<T>(v[qi] + bv));
                                 } else {
-                                    const uint32_t w2 = held[r < SW - 1 ? r : 0][c * (Sh::CQ / 2) + qi / 2];
+                                    // held step of residue r: 0 for SW = 2, r otherwise
+                                    const int hs = SW == 2 ? 0 : (r < SW - 1 ? r : 0);
+                                    const uint32_t w2 = held[hs][c * (Sh::CQ / 2) + qi / 2];
                                     two[e] = (qi & 1) ? (w2 >> 16) : (w2 & 0xFFFFu);
                                 }
                             }
