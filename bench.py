@@ -47,6 +47,8 @@ METRIC = "ConvTranspose TFLOP/s and HBM GB/s per config, as fraction of GB300 ro
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # fp32 FMA pipe: 152 SMs x 128 lanes x 2 flop x 2070 MHz maximum SM clock
 FP32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2070e6 / 1e12
+# nominal dense TF32 / BF16 tensor rates (1.1 and 2.25 PFLOP/s per GPU)
+TF32_PER_BF16 = 1.1 / 2.25
 FLUSH_BYTES = 512 << 20
 
 
@@ -103,7 +105,17 @@ ROUTE_KERNEL = {
     "grouped": ("grouped_staged_kernel", "hbm", "ct_grouped.cu"),
     "simt_gemm": ("simt_phase_gemm", "alu", "ct_simt.cu"),
     "tc_gemm": ("tc_phase_gemm", "tensor", "ct_tc.cu"),
+    "tc32_gemm": ("tc32_phase_gemm", "tensor", "ct_tc32.cu"),
     "bias_fill": ("bias_fill_kernel", "hbm", "ct_gather.cu"),
+}
+
+
+# How each route computes (the JSON line's dtype is the operand/output type).
+ARITHMETIC = {
+    "tc32_gemm": "f32 operands split into TF32 hi + lo; hi*hi + hi*lo + lo*hi on tcgen05 "
+                 "kind::tf32, fp32 accumulation",
+    "simt_gemm": "f32 FMA",
+    "tc_gemm": "bf16/f16 operands, fp32 accumulation on tcgen05 kind::f16",
 }
 
 
@@ -135,18 +147,27 @@ def roofline(route_name, p, main_ms, peaks, timed_alone):
     if bound == "tensor":
         peak = peaks["bf16_tflops"] if timed_alone else peaks.get("bf16_tflops_sustained",
                                                                   peaks["bf16_tflops"])
+        basis = "bf16 tensor peak"
+        if route_name == "tc32_gemm":
+            # three TF32 products per fp32 product: the fp32 work rate the
+            # TF32 pipe can sustain is a third of its peak
+            peak = peak * TF32_PER_BF16 / 3.0
+            basis = "bf16 tensor peak x nominal tf32/bf16 (1.1/2.25) / 3 TF32 products per fp32 product"
         achieved = flops / (main_ms * 1e-3) / 1e12
         unit = "TFLOP/s"
     elif bound == "alu":
         peak = FP32_ALU_PEAK_TFLOPS
+        basis = "nominal fp32 FMA: 152 SMs x 128 lanes x 2 flop x 2070 MHz"
         achieved = flops / (main_ms * 1e-3) / 1e12
         unit = "TFLOP/s"
     else:
         peak = peaks["hbm_gbs"]
+        basis = "HBM copy bandwidth"
         achieved = nbytes / (main_ms * 1e-3) / 1e9
         unit = "GB/s"
     return {"bound": bound, "kernel": kernel, "achieved": round(achieved, 3),
             "peak": round(peak, 3), "unit": unit, "frac": round(achieved / peak, 4),
+            "peak_basis": basis,
             "traffic": traffic_for(kernel, src, p.name),
             "algorithmic_bytes": nbytes, "algorithmic_flop": flops}
 
@@ -395,7 +416,7 @@ def run_ours(args):
     h2d, d2h = r.h2d_d2h_bytes()
 
     rl = roofline(route_name, p, main, peaks, timed_alone=True)
-    rl["peak_source"] = peak_src
+    rl["peak_source"] = "nominal" if rl["bound"] == "alu" else peak_src
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "TFLOP/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(ms, 5), "higher_is_better": True,
@@ -405,6 +426,7 @@ def run_ours(args):
                    "pad_lo": list(p.pad_lo), "pad_hi": list(p.pad_hi),
                    "dilation": list(p.dilation), "output_padding": list(p.output_padding),
                    "groups": p.groups, "bias": p.bias, "route": route_name,
+                   "arithmetic": ARITHMETIC.get(route_name, p.dtype),
                    "l2": "flushed between timed steps (512 MiB write)" if flush is not None
                    else "not flushed", "parallelism": f"replicas x{world}"},
         "hbm_gbs": round(world * nbytes / (ms * 1e-3) / 1e9, 2),

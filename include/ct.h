@@ -87,7 +87,13 @@ typedef enum {
     CT_ROUTE_GATHER = 2,    /* generic CUDA-core gather, any shape and dtype */
     CT_ROUTE_GROUPED = 3,   /* CUDA-core grouped/depthwise stride-phase gather */
     CT_ROUTE_SIMT_GEMM = 4, /* fp32 stride-phase implicit GEMM on CUDA cores */
-    CT_ROUTE_TC_GEMM = 5    /* bf16/fp16 stride-phase implicit GEMM on tcgen05 */
+    CT_ROUTE_TC_GEMM = 5,   /* bf16/fp16 stride-phase implicit GEMM on tcgen05 */
+    CT_ROUTE_TC32_GEMM = 6  /* fp32 stride-phase implicit GEMM on tcgen05 with
+                               error-compensated TF32: each operand split into
+                               TF32 hi + lo parts, products accumulated as
+                               hi*hi + hi*lo + lo*hi in fp32 (about fp32
+                               accuracy; CT_ROUTE_SIMT_GEMM is the plain fp32
+                               FMA route) */
 } ct_route;
 
 /* Library version (major*10000 + minor*100 + patch). */
@@ -271,11 +277,12 @@ int ct_conv_transpose_nd_noalloc(const void* x, const void* w, const void* bias,
                                  int groups, int dtype, void* stream);
 
 /*
- * Device-side error word written by bounded waits in the tensor-core kernel
- * (0 = none; otherwise the code says which wait gave up).  Synchronises the
- * current device, writes the word to *code and clears it when `clear` is
- * nonzero.  Returns CT_ERR_DEVICE_TIMEOUT when the word was set, CT_OK
- * otherwise.
+ * Device-side error word written by bounded waits in the tensor-core kernels
+ * (0 = none; otherwise the bits say which wait gave up: 1 producer, 2 MMA
+ * issuer, 4 epilogue, 8 drain after a failure; the words of the bf16/fp16
+ * and the fp32 tensor-core kernels are OR-ed).  Synchronises the current
+ * device, writes the word to *code and clears it when `clear` is nonzero.
+ * Returns CT_ERR_DEVICE_TIMEOUT when the word was set, CT_OK otherwise.
  */
 int ct_device_status(int clear, unsigned int* code);
 

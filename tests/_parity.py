@@ -58,7 +58,8 @@ def supported_routes(p):
     """Routes (besides AUTO) that can run problem p on this device."""
     out = []
     for r in (ct.CT_ROUTE_GATHER, ct.CT_ROUTE_GROUPED, ct.CT_ROUTE_SIMT_GEMM,
-              ct.CT_ROUTE_TC_GEMM, ct.CT_ROUTE_BIAS_FILL, ct.CT_ROUTE_NONE):
+              ct.CT_ROUTE_TC_GEMM, ct.CT_ROUTE_TC32_GEMM, ct.CT_ROUTE_BIAS_FILL,
+              ct.CT_ROUTE_NONE):
         try:
             ct.ct_conv_transpose_workspace_bytes(p.B, p.C_in, p.C_out, p.spatial, p.k, p.stride,
                                                  p.pad_lo, p.pad_hi, p.dilation,

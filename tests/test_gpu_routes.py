@@ -79,7 +79,7 @@ def test_grouped_route_matches_oracle(p):
 
 
 def test_auto_routes_of_the_workloads():
-    want = {0: ct.CT_ROUTE_GROUPED, 1: ct.CT_ROUTE_SIMT_GEMM, 2: ct.CT_ROUTE_TC_GEMM,
+    want = {0: ct.CT_ROUTE_GROUPED, 1: ct.CT_ROUTE_TC32_GEMM, 2: ct.CT_ROUTE_TC_GEMM,
             3: ct.CT_ROUTE_GROUPED, 4: ct.CT_ROUTE_TC_GEMM}
     for i, r in want.items():
         p = synth.workload(i)

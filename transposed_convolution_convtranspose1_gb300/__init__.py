@@ -7,7 +7,8 @@ library has not been built.  There is no CPU fallback.
 """
 from .ct import (  # noqa: F401
     CT_BF16, CT_F16, CT_F32, CT_OK, CT_ROUTE_AUTO, CT_ROUTE_BIAS_FILL, CT_ROUTE_GATHER,
-    CT_ROUTE_GROUPED, CT_ROUTE_NONE, CT_ROUTE_SIMT_GEMM, CT_ROUTE_TC_GEMM, EXPORTS,
+    CT_ROUTE_GROUPED, CT_ROUTE_NONE, CT_ROUTE_SIMT_GEMM, CT_ROUTE_TC_GEMM,
+    CT_ROUTE_TC32_GEMM, EXPORTS,
     ROUTE_NAMES, CtError, conv_transpose, ct_conv_transpose_nd, ct_conv_transpose_nd_host, ct_conv_transpose_nd_profiled,
     ct_conv_transpose_nd_noalloc, CT_NOALLOC_SCRATCH_BYTES,
     ct_conv_transpose_out_shape, ct_conv_transpose_route, ct_conv_transpose_workspace_bytes,

@@ -118,6 +118,7 @@ bool route_supports(const Problem& p, int route) {
         case CT_ROUTE_GROUPED: return !empty_out && !no_input && grouped_supports(p);
         case CT_ROUTE_SIMT_GEMM: return !empty_out && !no_input && simt_supports(p);
         case CT_ROUTE_TC_GEMM: return !empty_out && !no_input && tc_supports(p);
+        case CT_ROUTE_TC32_GEMM: return !empty_out && !no_input && tc32_supports(p);
         default: return false;
     }
 }
@@ -126,6 +127,7 @@ int choose_route(const Problem& p) {
     if (p.y_elems() == 0) return CT_ROUTE_NONE;
     if (p.C_in == 0 || p.in_spatial() == 0) return CT_ROUTE_BIAS_FILL;
     if (route_supports(p, CT_ROUTE_TC_GEMM) && tc_preferred(p)) return CT_ROUTE_TC_GEMM;
+    if (route_supports(p, CT_ROUTE_TC32_GEMM) && tc32_preferred(p)) return CT_ROUTE_TC32_GEMM;
     if (route_supports(p, CT_ROUTE_SIMT_GEMM) && simt_preferred(p)) return CT_ROUTE_SIMT_GEMM;
     if (route_supports(p, CT_ROUTE_GROUPED) && grouped_preferred(p)) return CT_ROUTE_GROUPED;
     return CT_ROUTE_GATHER;
@@ -135,6 +137,7 @@ size_t route_workspace(const Problem& p, int route) {
     switch (route) {
         case CT_ROUTE_SIMT_GEMM: return simt_workspace_bytes(p);
         case CT_ROUTE_TC_GEMM: return tc_workspace_bytes(p);
+        case CT_ROUTE_TC32_GEMM: return tc32_workspace_bytes(p);
         default: return 0;
     }
 }
@@ -164,6 +167,7 @@ int run(const Problem& p, int route, const void* x, const void* w, const void* b
         case CT_ROUTE_GROUPED: e = launch_grouped(p, x, w, bias, y, stream, prof); break;
         case CT_ROUTE_SIMT_GEMM: e = launch_simt(p, x, w, bias, y, ws, stream, prof); break;
         case CT_ROUTE_TC_GEMM: e = launch_tc(p, x, w, bias, y, ws, stream, prof); break;
+        case CT_ROUTE_TC32_GEMM: e = launch_tc32(p, x, w, bias, y, ws, stream, prof); break;
         default: e = cudaErrorInvalidValue; break;
     }
     if (owned) {
@@ -425,3 +429,13 @@ int ct_conv_transpose_nd_host(const void* x, const void* w, const void* bias, vo
 }
 
 }  // extern "C"
+
+extern "C" int ct_device_status(int clear, unsigned int* code) {
+    unsigned int a = 0, b = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = ct::tc_error_word(&a, clear != 0);
+    if (e == cudaSuccess) e = ct::tc32_error_word(&b, clear != 0);
+    if (code) *code = a | b;
+    if (e != cudaSuccess) return ct::report_error(CT_ERR_CUDA, "%s", cudaGetErrorString(e));
+    return (a | b) ? CT_ERR_DEVICE_TIMEOUT : CT_OK;
+}

@@ -26,4 +26,17 @@ size_t tc_workspace_bytes(const Problem& p);
 cudaError_t launch_tc(const Problem& p, const void* x, const void* w, const void* bias, void* y,
                       void* workspace, cudaStream_t stream, Profile* prof);
 
+// fp32 stride-phase implicit GEMM on tcgen05 tensor cores, error-compensated
+// TF32 (ct_tc32.cu).
+bool tc32_supports(const Problem& p);
+bool tc32_preferred(const Problem& p);
+size_t tc32_workspace_bytes(const Problem& p);
+cudaError_t launch_tc32(const Problem& p, const void* x, const void* w, const void* bias, void* y,
+                        void* workspace, cudaStream_t stream, Profile* prof);
+
+// Device error words of the tcgen05 routes: codes recorded by bounded waits
+// that timed out (0 = none); `clear` resets a non-zero word.
+cudaError_t tc_error_word(unsigned int* v, bool clear);
+cudaError_t tc32_error_word(unsigned int* v, bool clear);
+
 }  // namespace ct

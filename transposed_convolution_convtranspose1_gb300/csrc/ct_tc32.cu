@@ -1,0 +1,678 @@
+// ct_tc32.cu -- fp32 stride-phase implicit GEMM on tcgen05 tensor cores with
+// error-compensated TF32 ("3xTF32").
+//
+// Method.  The same stride-phase decomposition as the bf16/fp16 route: within
+// phase (r_d, r_h, r_w) every output o = r + s*q receives the taps T_r, each
+// reading input i = q + off(r, t), so the phase is the dense GEMM
+//     Y_r[b, oc, q] = sum_{t in T_r, ic} W[t][oc][ic] * X[b, q + off(r,t), ic]
+// (the ONNX page's implicit-gather GEMM with tap-reversed weights,
+// ai.onnx.ConvTranspose variant ncdhw3d_implicit_sgmat, per stride phase).
+//
+// fp32 on TF32 tensor cores.  Every fp32 operand v is split into two TF32
+// values, hi = v rounded to TF32 (10 explicit mantissa bits, round to nearest
+// even) and lo = (v - hi) rounded to TF32; v - hi is exact in fp32 and
+// |v - hi - lo| <= 2^-22 |v|.  A product is then accumulated as
+//     x*w ~= xh*wh + xh*wl + xl*wh
+// with three kind::tf32 MMAs into one fp32 TMEM accumulator; each TF32 x TF32
+// product is exact in fp32 and the dropped xl*wl is below 2^-22 |x w|, so a
+// sum of K products carries about the same error as an fp32 FMA chain.
+//
+// Kernels:
+//   1. tc32_weight_split    : w [C_in, C_out, taps] -> W'' [2][taps][N_pad][C_pad]
+//                             (plane 0 = hi, plane 1 = lo; K-major A operand)
+//   2. tc32_channels_last   : x [B, C, D*H*W] -> X'' [2][B][D*H*W][C_pad]
+//                             (hi, lo; K-major B operand, channels innermost so
+//                             that TMA boxes shift along the spatial axes only)
+//   3. tc32_phase_gemm      : persistent, warp-specialised, one CTA per SM.
+//        A tile is one stride phase x 128 output channels x NP positions.
+//        warp 0      TMA producer: per k-block (one tap, 32 input channels)
+//                    the hi and lo boxes of W'' and of X'' into a ring of
+//                    128-byte-swizzled stages
+//        warp 1      TMEM allocator and single-thread MMA issuer: 12
+//                    kind::tf32 MMAs per k-block (4 K-steps of 8 x 3 terms),
+//                    M = 128, N = NP.  The reduction runs in chunks of
+//                    kChunkKB k-blocks (128 channels of one tap), each into a
+//                    fresh accumulator; two accumulators of NP columns
+//                    alternate between chunks
+//        warps 2..9  epilogue: warp w reads TMEM lane quarter w % 4 (32 output
+//                    channels) and half of the NP positions; it adds each
+//                    chunk's partial sums into fp32 registers (round to
+//                    nearest) and, after a tile's last chunk, adds the bias
+//                    and writes 32 x 32 blocks (channels x positions) through
+//                    shared memory so that each warp store covers 32
+//                    consecutive q of one output row (outputs s_w apart).
+//      Why chunks: the tensor core's fp32 accumulation loses up to about an
+//      ulp of the running sum per MMA, an error that grows with the reduction
+//      depth times |y| (measured: 1.6e-5 of max|y| at 2048 products, above
+//      fp32 accuracy).  Restarting the accumulator every 128 channels bounds
+//      the running sum it rounds, and the chunk partials are summed with
+//      round-to-nearest fp32 adds in registers.
+//      Every mbarrier wait is bounded: on time-out the kernel records a code
+//      in its device error word, stops issuing work, drains its outstanding
+//      copies and MMAs (bounded too), frees TMEM and returns.
+#include <algorithm>
+#include <cstring>
+
+#include "ct_routes.h"
+#include "ct_tcgen05.cuh"
+
+namespace ct {
+
+namespace {
+
+using namespace tcg;
+
+constexpr int kMaxS = 8;          // stride per axis on this route
+constexpr int kMaxTaps = 8;       // taps per axis and phase on this route
+constexpr int kMaxClasses = 64;   // stride phases (r_d, r_h, r_w)
+constexpr int kBlockM = 128;      // output channels per tile (TMEM lanes)
+constexpr int kBlockK = 32;       // fp32 channels per k-block (one 128-byte row)
+constexpr int kNP = 256;          // positions per tile (MMA N)
+constexpr int kChunkKB = 4;       // k-blocks per TMEM accumulation chunk (128 channels)
+constexpr int kEpiWarps = 8;      // epilogue warps (two per TMEM lane quarter)
+constexpr int kEpiCols = kNP / 2; // positions per epilogue warp
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr uint32_t kPlaneA = kBlockM * kBlockK * 4;  // one A plane of a stage (16 KiB)
+
+struct Tc32Class {
+    int rd, rh, rw;         // residues on D, H, W
+    int start, count;       // tile index range
+    int n_qd, n_qh_blk, n_qw_blk;
+    int qd_ext, qh_ext, qw_ext;
+    int taps;               // taps of this phase (product over the axes)
+};
+
+struct Tc32Params {
+    CUtensorMap tmap_w;     // W'' as 3-D (C_pad, N_pad, 2 * taps)
+    CUtensorMap tmap_x;     // X'' as 5-D (C_pad, W, H, D, 2 * B)
+    const float* bias;
+    float* y;
+    int B, C_out, n_kblk, n_oc_tiles, taps;
+    int O[3];
+    int S[3];
+    int Kdims[3];
+    int WC, MR;             // tile positions = MR rows of WC positions along W
+    int ntap[3][kMaxS];
+    int tap[3][kMaxS][kMaxTaps];
+    int off[3][kMaxS][kMaxTaps];
+    int n_classes, total_tiles;
+    Tc32Class cls[kMaxClasses];
+    int stages;
+    uint32_t stage_bytes;
+    uint32_t idesc;
+    uint32_t tmem_cols;
+    uint32_t epi_off;       // offset of the epilogue blocks from the ring
+};
+
+struct Tile {
+    int cls, b, qd, qh0, qw0, oc0;
+};
+
+__device__ __forceinline__ Tile decode_tile(const Tc32Params& P, int t) {
+    int c = 0;
+    while (c + 1 < P.n_classes && t >= P.cls[c + 1].start) ++c;
+    const Tc32Class& C = P.cls[c];
+    int local = t - C.start;
+    Tile T;
+    T.cls = c;
+    const int oc_t = local % P.n_oc_tiles; local /= P.n_oc_tiles;
+    const int qw_b = local % C.n_qw_blk; local /= C.n_qw_blk;
+    const int qh_b = local % C.n_qh_blk; local /= C.n_qh_blk;
+    T.qd = local % C.n_qd;
+    T.b = local / C.n_qd;
+    T.qh0 = qh_b * P.MR;
+    T.qw0 = qw_b * P.WC;
+    T.oc0 = oc_t * kBlockM;
+    return T;
+}
+
+// ---------------------------------------------------------------------------
+// the GEMM kernel
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_constant__ Tc32Params P) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint64_t full_bar[8], empty_bar[8], sfull_bar[2], sempty_bar[2], drain_bar;
+    __shared__ uint32_t tmem_base_slot;
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t planeB = (uint32_t)kNP * kBlockK * 4;  // one B plane of a stage
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < P.stages; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&sfull_bar[b]), 1);
+            mbar_init(smem_u32(&sempty_bar[b]), kEpiWarps * 32);
+        }
+        mbar_init(smem_u32(&drain_bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_w))
+                     : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_x))
+                     : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&tmem_base_slot)),
+                     "r"(P.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_base_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+            const Tile tl = decode_tile(P, t);
+            const Tc32Class& C = P.cls[tl.cls];
+            const int nd_ = P.ntap[0][C.rd], nh_ = P.ntap[1][C.rh], nw_ = P.ntap[2][C.rw];
+            for (int jd = 0; jd < nd_ && ok; ++jd)
+                for (int jh = 0; jh < nh_ && ok; ++jh)
+                    for (int jw = 0; jw < nw_ && ok; ++jw) {
+                        const int tap =
+                            (P.tap[0][C.rd][jd] * P.Kdims[1] + P.tap[1][C.rh][jh]) * P.Kdims[2] +
+                            P.tap[2][C.rw][jw];
+                        const int id = tl.qd + P.off[0][C.rd][jd];
+                        const int ih = tl.qh0 + P.off[1][C.rh][jh];
+                        const int iw = tl.qw0 + P.off[2][C.rw][jw];
+                        for (int kb = 0; kb < P.n_kblk; ++kb) {
+                            ok = __all_sync(0xffffffffu,
+                                            mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1,
+                                                      kErrProducer, &abort_flag));
+                            if (!ok) break;
+                            if (lane == 0) {
+                                const uint32_t fb = smem_u32(&full_bar[stage]);
+                                const uint32_t sa = ring + stage * P.stage_bytes;
+                                mbar_expect_tx(fb, P.stage_bytes);
+                                tma_load_3d(sa, &P.tmap_w, fb, kb * kBlockK, tl.oc0, tap);
+                                tma_load_3d(sa + kPlaneA, &P.tmap_w, fb, kb * kBlockK, tl.oc0,
+                                            P.taps + tap);
+                                tma_load_5d(sa + 2 * kPlaneA, &P.tmap_x, fb, kb * kBlockK, iw, ih,
+                                            id, tl.b);
+                                tma_load_5d(sa + 2 * kPlaneA + planeB, &P.tmap_x, fb, kb * kBlockK,
+                                            iw, ih, id, P.B + tl.b);
+                            }
+                            __syncwarp();
+                            ++issued;
+                            if (++stage == P.stages) {
+                                stage = 0;
+                                phase ^= 1;
+                            }
+                        }
+                    }
+        }
+        if (!ok && lane == 0) {
+            // every copy issued so far must land before the CTA exits
+            const uint32_t first = issued > (uint32_t)P.stages ? issued - P.stages : 0;
+            for (uint32_t k = first; k < issued; ++k)
+                mbar_drain(smem_u32(&full_bar[k % P.stages]), (k / P.stages) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, chunk_iter = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+                const Tile tl = decode_tile(P, t);
+                const Tc32Class& C = P.cls[tl.cls];
+                const int nk = C.taps * P.n_kblk;
+                for (int k0 = 0; k0 < nk && ok; k0 += kChunkKB) {
+                    const int slot = (int)(chunk_iter & 1);
+                    const uint32_t use = chunk_iter >> 1;
+                    if (!mbar_wait(smem_u32(&sempty_bar[slot]), (use & 1) ^ 1, kErrMma,
+                                   &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + slot * kNP;
+                    const int k1 = min(nk, k0 + kChunkKB);
+                    for (int j = k0; j < k1; ++j) {
+                        if (!mbar_wait(smem_u32(&full_bar[stage]), phase, kErrMma, &abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t sa = ring + stage * P.stage_bytes;
+                        const uint64_t ah = smem_desc_sw128(sa);
+                        const uint64_t al = smem_desc_sw128(sa + kPlaneA);
+                        const uint64_t bh = smem_desc_sw128(sa + 2 * kPlaneA);
+                        const uint64_t bl = smem_desc_sw128(sa + 2 * kPlaneA + planeB);
+#pragma unroll
+                        for (int k = 0; k < kBlockK / 8; ++k) {
+                            // K-step of 8 TF32 elements = 32 bytes (encoded >> 4: 2)
+                            const uint64_t o = 2 * k;
+                            mma_tf32(d, al + o, bh + o, P.idesc, (j > k0 || k > 0) ? 1u : 0u);
+                            mma_tf32(d, ah + o, bl + o, P.idesc, 1u);
+                            mma_tf32(d, ah + o, bh + o, P.idesc, 1u);
+                        }
+                        mma_commit(smem_u32(&empty_bar[stage]));
+                        if (++stage == P.stages) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(smem_u32(&sfull_bar[slot]));
+                    ++chunk_iter;
+                }
+            }
+            // no MMA may be in flight when TMEM is released
+            mma_commit(smem_u32(&drain_bar));
+            mbar_drain(smem_u32(&drain_bar), 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        // Warp w reads TMEM lane quarter q = w % 4 (output channels
+        // oc0 + 32q .. +31, one per lane) and positions [h * 128, h * 128 + 128)
+        // of the tile, h = (w - 2) / 4.
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        // 32 x 32 block, column index XOR-swizzled by row: conflict-free both
+        // when a lane writes its row and when a lane reads a column
+        float* stg = reinterpret_cast<float*>(smem_raw + (P.epi_off + (ring - smem_u32(smem_raw)))) +
+                     (warp - 2) * 32 * 32;
+        uint32_t chunk_iter = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+            const Tile tl = decode_tile(P, t);
+            const Tc32Class& C = P.cls[tl.cls];
+            const int nk = C.taps * P.n_kblk;
+            const int od = C.rd + P.S[0] * tl.qd;
+            const bool d_ok = tl.qd < C.qd_ext;
+            // column group c (32 positions) of this warp lies in one output row
+            auto group_valid = [&](int c, int& qh, int& qwb) {
+                const int p0 = h * kEpiCols + c * 32;
+                qh = tl.qh0 + p0 / P.WC;
+                qwb = tl.qw0 + (p0 % P.WC);
+                return d_ok && qh < C.qh_ext && qwb < C.qw_ext;
+            };
+            float acc[kEpiCols];
+#pragma unroll
+            for (int i = 0; i < kEpiCols; ++i) acc[i] = 0.f;
+            for (int k0 = 0; k0 < nk; k0 += kChunkKB) {
+                const int slot = (int)(chunk_iter & 1);
+                const uint32_t use = chunk_iter >> 1;
+                ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sfull_bar[slot]), use & 1,
+                                                       kErrEpilogue, &abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t col0 = tmem_base + ((uint32_t)(q * 32) << 16) + slot * kNP + h * kEpiCols;
+                // every column is read (columns past the output only feed
+                // sums that are never stored); 16 per load keeps acc in registers
+#pragma unroll
+                for (int c = 0; c < kEpiCols / 16; ++c) {
+                    float v[16];
+                    tmem_ld16(col0 + c * 16, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[c * 16 + i] += v[i];
+                }
+                tc_fence_before();
+                mbar_arrive(smem_u32(&sempty_bar[slot]));
+                ++chunk_iter;
+            }
+            if (!ok) break;
+            const int oc_lane = tl.oc0 + q * 32 + lane;
+            const float bv = (P.bias != nullptr && oc_lane < P.C_out) ? P.bias[oc_lane] : 0.f;
+            const int64_t plane = (int64_t)P.O[0] * P.O[1];
+            const int n_oc = min(32, P.C_out - (tl.oc0 + q * 32));
+#pragma unroll
+            for (int c = 0; c < kEpiCols / 32; ++c) {
+                int qh, qwb;
+                if (!group_valid(c, qh, qwb)) continue;  // warp-uniform
+                // lane = channel: row `lane` of the block
+#pragma unroll
+                for (int i = 0; i < 32; ++i) stg[lane * 32 + (i ^ lane)] = acc[c * 32 + i] + bv;
+                __syncwarp();
+                // lane = position: column `lane`, one output row per channel
+                const int oh = C.rh + P.S[1] * qh;
+                const int qw = qwb + lane;
+                const int64_t ow = (int64_t)C.rw + (int64_t)P.S[2] * qw;
+                if (qw < C.qw_ext) {
+                    float* dst = P.y +
+                                 ((((int64_t)tl.b * P.C_out + tl.oc0 + q * 32) * P.O[0] + od) * P.O[1] + oh) *
+                                     P.O[2] + ow;
+                    const int64_t step = plane * P.O[2];
+                    for (int i = 0; i < n_oc; ++i, dst += step) *dst = stg[i * 32 + (lane ^ i)];
+                }
+                __syncwarp();
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(P.tmem_cols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
+// operand split and layout kernels
+// ---------------------------------------------------------------------------
+
+// v rounded to TF32 (10 explicit mantissa bits), round to nearest even; a
+// value that would round up past the largest finite float is truncated
+// instead, and inf / NaN pass through.
+__device__ __forceinline__ float tf32_rne(float v) {
+    const uint32_t u = __float_as_uint(v);
+    if ((u & 0x7F800000u) == 0x7F800000u) return v;
+    uint32_t r = (u + 0x0FFFu + ((u >> 13) & 1u)) & 0xFFFFE000u;
+    if ((r & 0x7F800000u) == 0x7F800000u) r = u & 0xFFFFE000u;
+    return __uint_as_float(r);
+}
+
+__device__ __forceinline__ void split_tf32(float v, float& hi, float& lo) {
+    hi = tf32_rne(v);
+    lo = tf32_rne(v - hi);
+}
+
+// W''[p][t][n][c] (p = 0 hi, 1 lo) from w[c][n][t]; zero for n >= C_out or
+// c >= C_in.  With j = n * taps + t, w is a [C_in][C_out * taps] matrix; a
+// block moves 32 channels x 256 consecutive j through a padded shared tile,
+// reading rows of w along j and writing W'' rows along c (128 bytes).
+__global__ void __launch_bounds__(256) tc32_weight_split(const float* __restrict__ w,
+                                                         float* __restrict__ wp, int C_in,
+                                                         int C_out, int taps, int N_pad,
+                                                         int C_pad) {
+    __shared__ float tile[32][257];
+    const int c0 = blockIdx.x * 32;
+    const int64_t j0 = (int64_t)blockIdx.y * 256;
+    const int64_t jn = (int64_t)C_out * taps;  // j of real output channels
+    const int64_t jt = (int64_t)N_pad * taps;  // j including the padded ones
+    for (int e = threadIdx.x; e < 32 * 256; e += 256) {
+        const int c = e / 256, jj = e % 256;
+        const int64_t j = j0 + jj;
+        tile[c][jj] = (c0 + c < C_in && j < jn) ? w[(int64_t)(c0 + c) * jn + j] : 0.f;
+    }
+    __syncthreads();
+    const int64_t plane = (int64_t)taps * N_pad * C_pad;
+    for (int e = threadIdx.x; e < 32 * 256; e += 256) {
+        const int c = e % 32, jj = e / 32;
+        const int64_t j = j0 + jj;
+        if (j >= jt) continue;
+        const int64_t n = j / taps, t = j % taps;
+        float hi, lo;
+        split_tf32(tile[c][jj], hi, lo);
+        const int64_t o = (t * N_pad + n) * C_pad + c0 + c;
+        wp[o] = hi;
+        wp[plane + o] = lo;
+    }
+}
+
+// X''[p][b][s][c] (p = 0 hi, 1 lo) from x[b][c][s]; zero for C <= c < C_pad.
+// Block: 32 channels x 32 positions through a padded shared tile; reads along
+// s and writes along c are both 128-byte rows.
+__global__ void __launch_bounds__(256) tc32_channels_last(const float* __restrict__ x,
+                                                          float* __restrict__ xc, int C, int C_pad,
+                                                          int64_t S, int B) {
+    __shared__ float tile[32][33];
+    const int64_t s0 = (int64_t)blockIdx.x * 32;
+    const int c0 = blockIdx.y * 32;
+    const int64_t b = blockIdx.z;
+    const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int c = ty + 8 * i;
+        const int64_t s = s0 + tx;
+        tile[c][tx] = (c0 + c < C && s < S) ? x[(b * C + c0 + c) * S + s] : 0.f;
+    }
+    __syncthreads();
+    const int64_t plane = (int64_t)B * S * C_pad;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int sl = ty + 8 * i;
+        const int64_t s = s0 + sl;
+        if (s >= S) continue;
+        float hi, lo;
+        split_tf32(tile[tx][sl], hi, lo);
+        const int64_t o = (b * S + s) * C_pad + c0 + tx;
+        xc[o] = hi;
+        xc[plane + o] = lo;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host planning
+// ---------------------------------------------------------------------------
+
+struct Tc32Plan {
+    int C_pad, N_pad, n_oc_tiles, WC, MR, stages;
+    size_t x_bytes, w_bytes, stage_bytes, epi_bytes;
+    AxisPlan ax[3];
+};
+
+constexpr size_t kSmemLimit = 232448;  // opt-in shared memory per block (227 KiB)
+
+bool make_plan(const Problem& p, Tc32Plan* pl) {
+    if (p.dtype != CT_F32) return false;
+    if (p.G != 1) return false;
+    for (int a = 0; a < 3; ++a) {
+        if (p.S[a] > kMaxS) return false;
+        plan_axis(p, a, &pl->ax[a]);
+        for (int r = 0; r < p.S[a]; ++r)
+            if (pl->ax[a].ntaps[r] > kMaxTaps) return false;
+    }
+    if (p.S[0] * p.S[1] * p.S[2] > kMaxClasses) return false;
+    pl->N_pad = (int)((p.C_out + kBlockM - 1) / kBlockM * kBlockM);
+    pl->n_oc_tiles = pl->N_pad / kBlockM;
+    pl->C_pad = (int)((p.C_in + kBlockK - 1) / kBlockK * kBlockK);
+    int64_t qw_max = 0;
+    for (int r = 0; r < p.S[2]; ++r) qw_max = std::max(qw_max, pl->ax[2].q_extent[r]);
+    int wc = 32;  // an epilogue block (32 positions) stays within one row
+    while (wc < qw_max && wc < kNP) wc *= 2;
+    pl->WC = wc;
+    pl->MR = kNP / wc;
+    pl->stage_bytes = 2 * (size_t)kPlaneA + 2 * (size_t)kNP * kBlockK * 4;
+    pl->epi_bytes = (size_t)kEpiWarps * 32 * 32 * 4;
+    const size_t room = kSmemLimit - 1024 - 1024 - pl->epi_bytes;
+    pl->stages = (int)std::min<size_t>(8, room / pl->stage_bytes);
+    if (pl->stages < 2) return false;
+    pl->x_bytes = 2 * (size_t)p.B * p.in_spatial() * pl->C_pad * 4;
+    pl->w_bytes = 2 * (size_t)p.taps() * pl->N_pad * pl->C_pad * 4;
+    // TMA limits: strides < 2^40, extents < 2^32; tile and class counts < 2^31
+    if ((double)p.in_spatial() * pl->C_pad * 4 * p.B >= 1e12) return false;
+    if (2 * p.B >= (1ll << 31) || 2 * p.taps() >= (1ll << 31)) return false;
+    return true;
+}
+
+cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x, const void* w,
+                             const void* bias, void* y, void* workspace, cudaStream_t stream,
+                             Profile* prof) {
+    DeviceInfo dev;
+    cudaError_t e = device_info(&dev);
+    if (e != cudaSuccess) return e;
+    char* ws = static_cast<char*>(workspace);
+    float* xc = reinterpret_cast<float*>(ws);
+    float* wp = reinterpret_cast<float*>(ws + round256(pl.x_bytes));
+
+    Tc32Params P;
+    std::memset(&P, 0, sizeof(P));
+    P.bias = static_cast<const float*>(bias);
+    P.y = static_cast<float*>(y);
+    P.B = (int)p.B;
+    P.C_out = (int)p.C_out;
+    P.n_kblk = pl.C_pad / kBlockK;
+    P.n_oc_tiles = pl.n_oc_tiles;
+    P.taps = (int)p.taps();
+    for (int a = 0; a < 3; ++a) {
+        P.O[a] = (int)p.O[a];
+        P.S[a] = p.S[a];
+        P.Kdims[a] = (int)p.K[a];
+        for (int r = 0; r < p.S[a]; ++r) {
+            P.ntap[a][r] = pl.ax[a].ntaps[r];
+            for (int j = 0; j < pl.ax[a].ntaps[r]; ++j) {
+                P.tap[a][r][j] = pl.ax[a].tap[r][j];
+                P.off[a][r][j] = pl.ax[a].off[r][j];
+            }
+        }
+    }
+    P.WC = pl.WC;
+    P.MR = pl.MR;
+    P.stages = pl.stages;
+    P.stage_bytes = (uint32_t)pl.stage_bytes;
+    P.tmem_cols = 2 * kNP;
+    P.idesc = (1u << 4)                              // D = f32
+              | (2u << 7)                            // A = tf32
+              | (2u << 10)                           // B = tf32
+              | ((uint32_t)(kNP >> 3) << 17)         // N = positions
+              | ((uint32_t)(kBlockM >> 4) << 24);    // M = output channels
+    P.epi_off = (uint32_t)(pl.stages * pl.stage_bytes);
+
+    // ---- tile classes (one per stride phase), heaviest first
+    Tc32Class hc[kMaxClasses];
+    int n = 0;
+    for (int rd = 0; rd < p.S[0]; ++rd)
+        for (int rh = 0; rh < p.S[1]; ++rh)
+            for (int rw = 0; rw < p.S[2]; ++rw) {
+                const int64_t qd = pl.ax[0].q_extent[rd], qh = pl.ax[1].q_extent[rh],
+                              qw = pl.ax[2].q_extent[rw];
+                if (qd == 0 || qh == 0 || qw == 0) continue;
+                Tc32Class c{};
+                c.rd = rd;
+                c.rh = rh;
+                c.rw = rw;
+                c.n_qd = (int)qd;
+                c.n_qh_blk = (int)((qh + pl.MR - 1) / pl.MR);
+                c.n_qw_blk = (int)((qw + pl.WC - 1) / pl.WC);
+                c.qd_ext = (int)qd;
+                c.qh_ext = (int)qh;
+                c.qw_ext = (int)qw;
+                c.taps = pl.ax[0].ntaps[rd] * pl.ax[1].ntaps[rh] * pl.ax[2].ntaps[rw];
+                const int64_t cnt =
+                    p.B * c.n_qd * (int64_t)c.n_qh_blk * c.n_qw_blk * pl.n_oc_tiles;
+                if (cnt >= (1ll << 31)) return cudaErrorInvalidValue;
+                c.count = (int)cnt;
+                hc[n++] = c;
+            }
+    std::stable_sort(hc, hc + n, [](const Tc32Class& a, const Tc32Class& b) { return a.taps > b.taps; });
+    int64_t total = 0;
+    for (int i = 0; i < n; ++i) {
+        hc[i].start = (int)total;
+        total += hc[i].count;
+    }
+    if (total >= (1ll << 31)) return cudaErrorInvalidValue;
+    P.n_classes = n;
+    P.total_tiles = (int)total;
+    for (int i = 0; i < n; ++i) P.cls[i] = hc[i];
+
+    // ---- tensor maps
+    auto enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)pl.C_pad, (cuuint64_t)pl.N_pad,
+                                    (cuuint64_t)(2 * p.taps())};
+        const cuuint64_t strides[2] = {(cuuint64_t)pl.C_pad * 4,
+                                       (cuuint64_t)pl.C_pad * 4 * pl.N_pad};
+        const cuuint32_t box[3] = {(cuuint32_t)kBlockK, (cuuint32_t)kBlockM, 1};
+        const cuuint32_t es[3] = {1, 1, 1};
+        CUresult r = enc(&P.tmap_w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, wp, dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[5] = {(cuuint64_t)pl.C_pad, (cuuint64_t)p.I[2], (cuuint64_t)p.I[1],
+                                    (cuuint64_t)p.I[0], (cuuint64_t)(2 * p.B)};
+        const cuuint64_t row = (cuuint64_t)pl.C_pad * 4;
+        const cuuint64_t strides[4] = {row, row * p.I[2], row * p.I[2] * p.I[1],
+                                       row * p.I[2] * p.I[1] * p.I[0]};
+        const cuuint32_t box[5] = {(cuuint32_t)kBlockK, (cuuint32_t)pl.WC, (cuuint32_t)pl.MR, 1, 1};
+        const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+        CUresult r = enc(&P.tmap_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, xc, dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+
+    // ---- launches
+    {
+        const int64_t jblk = ((int64_t)pl.N_pad * p.taps() + 255) / 256;
+        dim3 grid((unsigned)(pl.C_pad / 32), (unsigned)jblk);
+        if (jblk > 65535) return cudaErrorInvalidConfiguration;
+        tc32_weight_split<<<grid, 256, 0, stream>>>(static_cast<const float*>(w), wp, (int)p.C_in,
+                                                    (int)p.C_out, (int)p.taps(), pl.N_pad,
+                                                    pl.C_pad);
+        prof_count(prof);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    {
+        const int64_t S = p.in_spatial();
+        dim3 grid((unsigned)((S + 31) / 32), (unsigned)(pl.C_pad / 32), (unsigned)p.B);
+        if (grid.y > 65535 || grid.z > 65535 || (S + 31) / 32 >= (1ll << 31))
+            return cudaErrorInvalidConfiguration;
+        tc32_channels_last<<<grid, 256, 0, stream>>>(static_cast<const float*>(x), xc, (int)p.C_in,
+                                                     pl.C_pad, S, (int)p.B);
+        prof_count(prof);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    const size_t smem = (size_t)P.stages * P.stage_bytes + pl.epi_bytes + 1024;
+    const int grid = std::max(1, std::min(P.total_tiles, dev.sm_count));
+    e = cudaFuncSetAttribute(tc32_phase_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    prof_begin(prof, stream);
+    tc32_phase_gemm<<<grid, kThreads, smem, stream>>>(P);
+    e = cudaGetLastError();
+    prof_end(prof, stream);
+    prof_count(prof);
+    return e;
+}
+
+}  // namespace
+
+bool tc32_supports(const Problem& p) {
+    Tc32Plan pl;
+    if (!make_plan(p, &pl)) return false;
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess) return false;
+    return d.cc_major == 10 && d.cc_minor == 3;
+}
+
+bool tc32_preferred(const Problem& p) { return p.C_in >= 32 && p.C_out >= 32; }
+
+size_t tc32_workspace_bytes(const Problem& p) {
+    Tc32Plan pl;
+    if (!make_plan(p, &pl)) return 0;
+    return round256(pl.x_bytes) + round256(pl.w_bytes);
+}
+
+cudaError_t launch_tc32(const Problem& p, const void* x, const void* w, const void* bias, void* y,
+                        void* workspace, cudaStream_t stream, Profile* prof) {
+    Tc32Plan pl;
+    if (!make_plan(p, &pl)) return cudaErrorInvalidValue;
+    return launch_tc32_impl(p, pl, x, w, bias, y, workspace, stream, prof);
+}
+
+cudaError_t tc32_error_word(unsigned int* v, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(v, g_device_error, sizeof(*v));
+    if (e == cudaSuccess && clear && *v != 0) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+    }
+    return e;
+}
+
+}  // namespace ct

@@ -30,8 +30,9 @@ CT_ROUTE_GATHER = 2
 CT_ROUTE_GROUPED = 3
 CT_ROUTE_SIMT_GEMM = 4
 CT_ROUTE_TC_GEMM = 5
+CT_ROUTE_TC32_GEMM = 6
 ROUTE_NAMES = {0: "none", 1: "bias_fill", 2: "gather", 3: "grouped",
-               4: "simt_gemm", 5: "tc_gemm"}
+               4: "simt_gemm", 5: "tc_gemm", 6: "tc32_gemm"}
 
 _DTYPE_CODE = {torch.float32: CT_F32, torch.float16: CT_F16, torch.bfloat16: CT_BF16}
 # Any other torch dtype is passed as an out-of-range code, which the library
