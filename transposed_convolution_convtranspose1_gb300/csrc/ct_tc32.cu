@@ -25,11 +25,11 @@
 //                             that TMA boxes shift along the spatial axes only)
 //   3. tc32_phase_gemm      : persistent, warp-specialised, one CTA per SM.
 //        A tile is one stride phase x 128 output channels x NP positions.
-//        warp 0      TMA producer: per k-block (one tap, 32 input channels)
+//        warp 0      TMA producer: per k-block (one tap, 16 input channels)
 //                    the hi and lo boxes of W'' and of X'' into a ring of
-//                    128-byte-swizzled stages
-//        warp 1      TMEM allocator and single-thread MMA issuer: 12
-//                    kind::tf32 MMAs per k-block (4 K-steps of 8 x 3 terms),
+//                    64-byte-swizzled stages (48 KiB each, four in flight)
+//        warp 1      TMEM allocator and single-thread MMA issuer: 6
+//                    kind::tf32 MMAs per k-block (2 K-steps of 8 x 3 terms),
 //                    M = 128, N = NP.  The reduction runs in chunks of
 //                    kChunkKB k-blocks (128 channels of one tap), each into a
 //                    fresh accumulator; two accumulators of NP columns
@@ -66,13 +66,14 @@ constexpr int kMaxS = 8;          // stride per axis on this route
 constexpr int kMaxTaps = 8;       // taps per axis and phase on this route
 constexpr int kMaxClasses = 64;   // stride phases (r_d, r_h, r_w)
 constexpr int kBlockM = 128;      // output channels per tile (TMEM lanes)
-constexpr int kBlockK = 32;       // fp32 channels per k-block (one 128-byte row)
+constexpr int kBlockK = 16;       // fp32 channels per k-block (one 64-byte swizzled row)
+constexpr int kCAlign = 32;       // C_in padding (the layout pass moves 32-channel tiles)
 constexpr int kNP = 256;          // positions per tile (MMA N)
-constexpr int kChunkKB = 4;       // k-blocks per TMEM accumulation chunk (128 channels)
+constexpr int kChunkKB = 8;       // k-blocks per TMEM accumulation chunk (128 channels)
 constexpr int kEpiWarps = 8;      // epilogue warps (two per TMEM lane quarter)
 constexpr int kEpiCols = kNP / 2; // positions per epilogue warp
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr uint32_t kPlaneA = kBlockM * kBlockK * 4;  // one A plane of a stage (16 KiB)
+constexpr uint32_t kPlaneA = kBlockM * kBlockK * 4;  // one A plane of a stage (8 KiB)
 
 struct Tc32Class {
     int rd, rh, rw;         // residues on D, H, W
@@ -252,10 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
                             break;
                         }
                         const uint32_t sa = ring + stage * P.stage_bytes;
-                        const uint64_t ah = smem_desc_sw128(sa);
-                        const uint64_t al = smem_desc_sw128(sa + kPlaneA);
-                        const uint64_t bh = smem_desc_sw128(sa + 2 * kPlaneA);
-                        const uint64_t bl = smem_desc_sw128(sa + 2 * kPlaneA + planeB);
+                        const uint64_t ah = smem_desc_sw64(sa);
+                        const uint64_t al = smem_desc_sw64(sa + kPlaneA);
+                        const uint64_t bh = smem_desc_sw64(sa + 2 * kPlaneA);
+                        const uint64_t bl = smem_desc_sw64(sa + 2 * kPlaneA + planeB);
 #pragma unroll
                         for (int k = 0; k < kBlockK / 8; ++k) {
                             // K-step of 8 TF32 elements = 32 bytes (encoded >> 4: 2)
@@ -479,7 +480,7 @@ bool make_plan(const Problem& p, Tc32Plan* pl) {
     if (p.S[0] * p.S[1] * p.S[2] > kMaxClasses) return false;
     pl->N_pad = (int)((p.C_out + kBlockM - 1) / kBlockM * kBlockM);
     pl->n_oc_tiles = pl->N_pad / kBlockM;
-    pl->C_pad = (int)((p.C_in + kBlockK - 1) / kBlockK * kBlockK);
+    pl->C_pad = (int)((p.C_in + kCAlign - 1) / kCAlign * kCAlign);
     int64_t qw_max = 0;
     for (int r = 0; r < p.S[2]; ++r) qw_max = std::max(qw_max, pl->ax[2].q_extent[r]);
     int wc = 32;  // an epilogue block (32 positions) stays within one row
@@ -590,7 +591,7 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
         const cuuint32_t box[3] = {(cuuint32_t)kBlockK, (cuuint32_t)kBlockM, 1};
         const cuuint32_t es[3] = {1, 1, 1};
         CUresult r = enc(&P.tmap_w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, wp, dims, strides, box, es,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
@@ -603,7 +604,7 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
         const cuuint32_t box[5] = {(cuuint32_t)kBlockK, (cuuint32_t)pl.WC, (cuuint32_t)pl.MR, 1, 1};
         const cuuint32_t es[5] = {1, 1, 1, 1, 1};
         CUresult r = enc(&P.tmap_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, xc, dims, strides, box, es,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }

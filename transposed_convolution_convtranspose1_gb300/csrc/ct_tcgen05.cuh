@@ -152,6 +152,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
     return d;
 }
 
+// Shared-memory matrix descriptor: K-major, 64-byte swizzle, rows of 64
+// bytes, 8-row groups 512 bytes apart (SBO), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);       // start address
+    d |= (uint64_t)(16u >> 4) << 16;               // leading byte offset (unused here)
+    d |= (uint64_t)(512u >> 4) << 32;              // stride byte offset
+    d |= (uint64_t)1 << 46;                        // version
+    d |= (uint64_t)4 << 61;                        // SWIZZLE_64B
+    return d;
+}
+
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                         uint32_t idesc, uint32_t accumulate) {
     asm volatile(
