@@ -187,15 +187,25 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __
     // weights: slab[tap][ic][oc], CIGP x COGP per tap (zero padded)
     float* slab = sm;
     float* xs = sm + P.taps * CIGP * COGP;  // [jd * NR + r][p][CIGP]
+    // Loads are issued in batches (every load of a batch in flight before
+    // its stores), so that the block waits for global memory a few times
+    // rather than once per staged element.
+    constexpr int kSlabBatch = 4;
     const int slab_n = P.taps * CIGP * COGP;
-    for (int e = threadIdx.x; e < slab_n; e += blockDim.x) {
-        const int oc = e % COGP;
-        const int ic = (e / COGP) % CIGP;
-        const int t = e / (COGP * CIGP);
-        float v = 0.f;
-        if (oc < P.Cog && ic < P.Cig)
-            v = to_f32(w[((int64_t)(g * P.Cig + ic) * P.Cog + oc) * P.taps + t]);
-        slab[e] = v;
+    for (int e0 = threadIdx.x; e0 < slab_n; e0 += kSlabBatch * blockDim.x) {
+        float v[kSlabBatch];
+#pragma unroll
+        for (int k = 0; k < kSlabBatch; ++k) {
+            const int e = e0 + k * blockDim.x;
+            const int oc = e % COGP;
+            const int ic = (e / COGP) % CIGP;
+            const int t = e / (COGP * CIGP);
+            v[k] = (e < slab_n && oc < P.Cog && ic < P.Cig)
+                       ? to_f32(w[((int64_t)(g * P.Cig + ic) * P.Cog + oc) * P.taps + t]) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kSlabBatch; ++k)
+            if (e0 + k * blockDim.x < slab_n) slab[e0 + k * blockDim.x] = v[k];
     }
     const int64_t in_plane = (int64_t)P.I[0] * P.I[1] * P.I[2];
     const T* xg = x + (b * P.C_in + (int64_t)g * P.Cig) * in_plane;
@@ -206,20 +216,25 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __
         const int ih = ih_lo + r;
         const bool row_ok = id >= 0 && id < P.I[0] && ih >= 0 && ih < P.I[1];
         const T* src = xg + ((int64_t)id * P.I[1] + ih) * P.I[2];
+        // every slot of the row loaded before any is stored
+        float v[kGrpStageW][CIGP];
+#pragma unroll
+        for (int k = 0; k < kGrpStageW; ++k) {
+            const int pp = lane + 32 * k;
+            const int iw = pp + P.base_w;
+            const bool ok = row_ok && pp < WS && iw >= 0 && iw < P.I[2];
+#pragma unroll
+            for (int ic = 0; ic < CIGP; ++ic)
+                v[k][ic] = (ok && ic < P.Cig) ? to_f32(src[(int64_t)ic * in_plane + iw]) : 0.f;
+        }
 #pragma unroll
         for (int k = 0; k < kGrpStageW; ++k) {
             const int pp = lane + 32 * k;
             if (pp >= WS) break;
-            const int iw = pp + P.base_w;
-            const bool ok = row_ok && iw >= 0 && iw < P.I[2];
-            float v[CIGP];
-#pragma unroll
-            for (int ic = 0; ic < CIGP; ++ic)
-                v[ic] = (ok && ic < P.Cig) ? to_f32(src[(int64_t)ic * in_plane + iw]) : 0.f;
             float4* dst = reinterpret_cast<float4*>(xs + ((int64_t)rowi * WS + pp) * xstride<CIGP>());
 #pragma unroll
             for (int c4 = 0; c4 < CIGP / 4; ++c4)
-                dst[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+                dst[c4] = make_float4(v[k][4 * c4], v[k][4 * c4 + 1], v[k][4 * c4 + 2], v[k][4 * c4 + 3]);
         }
     }
     __syncthreads();
