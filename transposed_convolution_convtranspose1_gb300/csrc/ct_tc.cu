@@ -8,16 +8,17 @@
 // over C_in x |T_r| -- the ONNX page's implicit-gather GEMM with tap-reversed
 // weights (ai.onnx.ConvTranspose, variant ncdhw3d_implicit_sgmat: no column
 // matrix, no scatter pass, reduction over the full in-channel-by-tap depth),
-// generalised from stride 1 to every stride phase.  Three kernels run:
-//   1. tc_weight_reorder : w [C_in, C_out, taps] -> W' [taps][N_pad][C_pad]
-//                          (K-major A operand, zero padded; taps indexed in the
-//                          pages' unflipped order, visited per phase in
-//                          reversed order, i.e. increasing input offset)
-//   2. tc_channels_last  : x [B, C, D*H*W] -> X' [B, D, H, W, C_pad]
+// generalised from stride 1 to every stride phase.  Two kernels run:
+//   1. tc_prepare        : one launch, two kinds of blocks:
+//        x [B, C, D*H*W] -> X' [B, D, H, W, C_pad]
 //                          (K-major B operand; TMA boxes then shift along the
 //                          spatial axes only, so every box starts on a
 //                          128-byte boundary of the channel axis)
-//   3. tc_phase_gemm     : persistent, warp-specialised, one CTA per SM:
+//        w [C_in, C_out, taps] -> W' [taps][N_pad][C_pad]
+//                          (K-major A operand, zero padded; taps indexed in the
+//                          pages' unflipped order, visited per phase in
+//                          reversed order, i.e. increasing input offset)
+//   2. tc_phase_gemm     : persistent, warp-specialised, one CTA per SM:
 //        warp 0      TMA producer: per k-block (one tap, 64 input channels)
 //                    a box of W' (128 output channels) and a 5-D box of X'
 //                    (NP output positions, shifted by the tap's input
@@ -510,19 +511,38 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
 // layout kernels
 // ---------------------------------------------------------------------------
 
-// W'[tap][n][c] = w[c][n][tap] for n < C_out, c < C_in, else 0.
+// W'[tap][n][c] = w[c][n][tap] for n < C_out, c < C_in, else 0.  With
+// j = n * taps + tap, w is a [C_in][C_out * taps] matrix; one block moves a
+// 64 (c) x 64 (j) tile through shared memory, reading rows of w along j and
+// writing rows of W' along c (128 bytes each), every load of a thread in
+// flight before its stores.
 template <typename T>
-__global__ void tc_weight_reorder(const T* __restrict__ w, T* __restrict__ wp, int C_in, int C_out,
-                                  int taps, int N_pad, int C_pad) {
-    const int64_t total = (int64_t)taps * N_pad * C_pad;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-         e += (int64_t)gridDim.x * blockDim.x) {
-        const int c = (int)(e % C_pad);
-        const int n = (int)((e / C_pad) % N_pad);
-        const int t = (int)(e / ((int64_t)C_pad * N_pad));
-        T v = from_f32<T>(0.f);
-        if (c < C_in && n < C_out) v = w[((int64_t)c * C_out + n) * taps + t];
-        wp[e] = v;
+__device__ __forceinline__ void tc_weight_tile(const T* __restrict__ w, T* __restrict__ wp, int C_in,
+                                               int C_out, int taps, int N_pad, int C_pad, int c0,
+                                               int64_t j0) {
+    __shared__ uint16_t tile[64][66];
+    const uint16_t* ws = reinterpret_cast<const uint16_t*>(w);
+    uint16_t* wd = reinterpret_cast<uint16_t*>(wp);
+    const int64_t jn = (int64_t)C_out * taps;  // j of real output channels
+    const int64_t jt = (int64_t)N_pad * taps;  // j including the padded ones
+    const int t = threadIdx.x;
+    uint16_t v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int c = t / 64 + 4 * i, jj = t % 64;
+        const int64_t j = j0 + jj;
+        v[i] = (c0 + c < C_in && j < jn) ? ws[(int64_t)(c0 + c) * jn + j] : (uint16_t)0;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) tile[t / 64 + 4 * i][t % 64] = v[i];
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int c = t % 64, jj = t / 64 + 4 * i;
+        const int64_t j = j0 + jj;
+        if (j >= jt) continue;
+        const int64_t n = j / taps, tp = j % taps;
+        wd[(tp * N_pad + n) * C_pad + c0 + c] = tile[c][jj];
     }
 }
 
@@ -533,12 +553,9 @@ __global__ void tc_weight_reorder(const T* __restrict__ w, T* __restrict__ wp, i
 // its 8-element column chunks XOR-swizzled by row so that both the scattered
 // 2-byte writes and the 16-byte row reads avoid bank conflicts.
 template <typename T>
-__global__ void __launch_bounds__(256) tc_channels_last(const T* __restrict__ x, T* __restrict__ xc,
-                                                        int C, int C_pad, int64_t S, bool vec) {
+__device__ __forceinline__ void tc_x_tile(const T* __restrict__ x, T* __restrict__ xc, int C, int C_pad,
+                                          int64_t S, bool vec, int64_t s0, int c0, int64_t b) {
     __shared__ __align__(16) uint16_t tile[64][64];
-    const int64_t s0 = (int64_t)blockIdx.x * 64;
-    const int c0 = blockIdx.y * 64;
-    const int64_t b = blockIdx.z;
     const uint16_t* xs = reinterpret_cast<const uint16_t*>(x);
     uint16_t* xd = reinterpret_cast<uint16_t*>(xc);
     const int t = threadIdx.x;
@@ -575,6 +592,34 @@ __global__ void __launch_bounds__(256) tc_channels_last(const T* __restrict__ x,
         const int key = (sl & 7) ^ (sl >> 3);
         const uint4 u = *reinterpret_cast<const uint4*>(&tile[sl][(cv ^ key) << 3]);
         *reinterpret_cast<uint4*>(xd + (b * S + s) * C_pad + c0 + cv * 8) = u;
+    }
+}
+
+// One launch prepares both GEMM operands: blocks [0, n_xb) move X' tiles
+// (s-tile fastest, then c-tile, then batch), the remaining blocks W' tiles.
+struct TcPrep {
+    const void* x; void* xc; const void* w; void* wp;
+    int C, C_pad, B, C_out, taps, N_pad;
+    int64_t S;
+    int n_st, n_ct, n_jt;  // x tiles along s and c; weight tiles along j
+    int64_t n_xb;
+    bool vec;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) tc_prepare(const __grid_constant__ TcPrep Q) {
+    const int64_t bid = blockIdx.x;
+    if (bid < Q.n_xb) {
+        const int64_t st = bid % Q.n_st, rest = bid / Q.n_st;
+        const int ct = (int)(rest % Q.n_ct);
+        const int64_t b = rest / Q.n_ct;
+        tc_x_tile<T>(static_cast<const T*>(Q.x), static_cast<T*>(Q.xc), Q.C, Q.C_pad, Q.S, Q.vec,
+                     st * 64, ct * 64, b);
+    } else {
+        const int64_t wb = bid - Q.n_xb;
+        const int jt = (int)(wb % Q.n_jt), ct = (int)(wb / Q.n_jt);
+        tc_weight_tile<T>(static_cast<const T*>(Q.w), static_cast<T*>(Q.wp), Q.C, Q.C_out, Q.taps,
+                          Q.N_pad, Q.C_pad, ct * 64, (int64_t)jt * 64);
     }
 }
 
@@ -772,22 +817,20 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
 
     // ---- launches
     {
-        const int64_t tot = p.taps() * pl.N_pad * pl.C_pad;
-        const int blocks = (int)std::min<int64_t>((tot + 255) / 256, (int64_t)dev.sm_count * 8);
-        tc_weight_reorder<T><<<blocks, 256, 0, stream>>>(static_cast<const T*>(w), wp, (int)p.C_in,
-                                                         (int)p.C_out, (int)p.taps(), pl.N_pad,
-                                                         pl.C_pad);
-        prof_count(prof);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    {
-        const int64_t S = p.in_spatial();
-        dim3 grid((unsigned)((S + 63) / 64), (unsigned)(pl.C_pad / 64), (unsigned)p.B);
-        if (grid.y > 65535 || grid.z > 65535) return cudaErrorInvalidConfiguration;
+        TcPrep Q;
+        Q.x = x; Q.xc = xc; Q.w = w; Q.wp = wp;
+        Q.C = (int)p.C_in; Q.C_pad = pl.C_pad; Q.B = (int)p.B; Q.C_out = (int)p.C_out;
+        Q.taps = (int)p.taps(); Q.N_pad = pl.N_pad;
+        Q.S = p.in_spatial();
+        Q.n_st = (int)((Q.S + 63) / 64);
+        Q.n_ct = pl.C_pad / 64;
+        Q.n_jt = (int)(((int64_t)pl.N_pad * p.taps() + 63) / 64);
+        Q.n_xb = (int64_t)Q.n_st * Q.n_ct * p.B;
         // 16-byte loads need S % 8 == 0 and a 16-byte aligned x
-        const bool vec = (S % 8) == 0 && ((uintptr_t)x % 16) == 0;
-        tc_channels_last<T><<<grid, 256, 0, stream>>>(static_cast<const T*>(x), xc, (int)p.C_in,
-                                                      pl.C_pad, S, vec);
+        Q.vec = (Q.S % 8) == 0 && ((uintptr_t)x % 16) == 0;
+        const int64_t blocks = Q.n_xb + (int64_t)Q.n_jt * Q.n_ct;
+        if ((Q.S + 63) / 64 >= (1ll << 31) || blocks >= (1ll << 31)) return cudaErrorInvalidConfiguration;
+        tc_prepare<T><<<(unsigned)blocks, 256, 0, stream>>>(Q);
         prof_count(prof);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

@@ -18,12 +18,13 @@
 // sum of K products carries about the same error as an fp32 FMA chain.
 //
 // Kernels:
-//   1. tc32_weight_split    : w [C_in, C_out, taps] -> W'' [2][taps][N_pad][C_pad]
+//   1. tc32_prepare         : one launch, two kinds of blocks:
+//        w [C_in, C_out, taps] -> W'' [2][taps][N_pad][C_pad]
 //                             (plane 0 = hi, plane 1 = lo; K-major A operand)
-//   2. tc32_channels_last   : x [B, C, D*H*W] -> X'' [2][B][D*H*W][C_pad]
+//        x [B, C, D*H*W] -> X'' [2][B][D*H*W][C_pad]
 //                             (hi, lo; K-major B operand, channels innermost so
 //                             that TMA boxes shift along the spatial axes only)
-//   3. tc32_phase_gemm      : persistent, warp-specialised, one CTA per SM.
+//   2. tc32_phase_gemm      : persistent, warp-specialised, one CTA per SM.
 //        A tile is one stride phase x 128 output channels x NP positions.
 //        warp 0      TMA producer: per k-block (one tap, 16 input channels)
 //                    the hi and lo boxes of W'' and of X'' into a ring of
@@ -392,67 +393,112 @@ __device__ __forceinline__ void split_tf32(float v, float& hi, float& lo) {
 }
 
 // W''[p][t][n][c] (p = 0 hi, 1 lo) from w[c][n][t]; zero for n >= C_out or
-// c >= C_in.  With j = n * taps + t, w is a [C_in][C_out * taps] matrix; a
-// block moves 32 channels x 256 consecutive j through a padded shared tile,
-// reading rows of w along j and writing W'' rows along c (128 bytes).
-__global__ void __launch_bounds__(256) tc32_weight_split(const float* __restrict__ w,
-                                                         float* __restrict__ wp, int C_in,
-                                                         int C_out, int taps, int N_pad,
-                                                         int C_pad) {
-    __shared__ float tile[32][257];
-    const int c0 = blockIdx.x * 32;
-    const int64_t j0 = (int64_t)blockIdx.y * 256;
+// c >= C_in.  With j = n * taps + t, w is a [C_in][C_out * taps] matrix; one
+// block moves 32 channels x 64 consecutive j through a padded shared tile,
+// reading rows of w along j and writing W'' rows along c (128 bytes), every
+// load of a thread in flight before its stores.
+__device__ __forceinline__ void tc32_weight_tile(const float* __restrict__ w, float* __restrict__ wp,
+                                                 int C_in, int C_out, int taps, int N_pad, int C_pad,
+                                                 int c0, int64_t j0) {
+    __shared__ float tile[32][65];
     const int64_t jn = (int64_t)C_out * taps;  // j of real output channels
     const int64_t jt = (int64_t)N_pad * taps;  // j including the padded ones
-    for (int e = threadIdx.x; e < 32 * 256; e += 256) {
-        const int c = e / 256, jj = e % 256;
+    const int t = threadIdx.x;
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int c = t / 64 + 4 * i, jj = t % 64;
         const int64_t j = j0 + jj;
-        tile[c][jj] = (c0 + c < C_in && j < jn) ? w[(int64_t)(c0 + c) * jn + j] : 0.f;
+        v[i] = (c0 + c < C_in && j < jn) ? __ldg(w + (int64_t)(c0 + c) * jn + j) : 0.f;
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) tile[t / 64 + 4 * i][t % 64] = v[i];
     __syncthreads();
     const int64_t plane = (int64_t)taps * N_pad * C_pad;
-    for (int e = threadIdx.x; e < 32 * 256; e += 256) {
-        const int c = e % 32, jj = e / 32;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int c = t % 32, jj = t / 32 + 8 * i;
         const int64_t j = j0 + jj;
         if (j >= jt) continue;
-        const int64_t n = j / taps, t = j % taps;
+        const int64_t n = j / taps, tp = j % taps;
         float hi, lo;
         split_tf32(tile[c][jj], hi, lo);
-        const int64_t o = (t * N_pad + n) * C_pad + c0 + c;
+        const int64_t o = (tp * N_pad + n) * C_pad + c0 + c;
         wp[o] = hi;
         wp[plane + o] = lo;
     }
 }
 
 // X''[p][b][s][c] (p = 0 hi, 1 lo) from x[b][c][s]; zero for C <= c < C_pad.
-// Block: 32 channels x 32 positions through a padded shared tile; reads along
-// s and writes along c are both 128-byte rows.
-__global__ void __launch_bounds__(256) tc32_channels_last(const float* __restrict__ x,
-                                                          float* __restrict__ xc, int C, int C_pad,
-                                                          int64_t S, int B) {
-    __shared__ float tile[32][33];
-    const int64_t s0 = (int64_t)blockIdx.x * 32;
-    const int c0 = blockIdx.y * 32;
-    const int64_t b = blockIdx.z;
-    const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+// One block moves 32 channels x 64 positions through a shared tile of odd
+// row pitch: 16-byte loads along s (when S % 4 == 0 and x is 16-byte
+// aligned), 16-byte stores of four channels along c; the column reads of
+// the tile fall on distinct banks.
+__device__ __forceinline__ void tc32_x_tile(const float* __restrict__ x, float* __restrict__ xc, int C,
+                                            int C_pad, int64_t S, int B, bool vec, int64_t s0, int c0,
+                                            int64_t b) {
+    __shared__ float tile[32][65];
+    const int t = threadIdx.x;
+    float4 v[2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int c = ty + 8 * i;
-        const int64_t s = s0 + tx;
-        tile[c][tx] = (c0 + c < C && s < S) ? x[(b * C + c0 + c) * S + s] : 0.f;
+    for (int i = 0; i < 2; ++i) {
+        const int c = t / 16 + 16 * i, s4 = t % 16;
+        const int64_t s = s0 + 4 * s4;
+        const float* src = x + (b * C + c0 + c) * S + s;
+        if (c0 + c < C && vec && s + 4 <= S) {
+            v[i] = __ldg(reinterpret_cast<const float4*>(src));
+        } else {
+            v[i].x = (c0 + c < C && s + 0 < S) ? src[0] : 0.f;
+            v[i].y = (c0 + c < C && s + 1 < S) ? src[1] : 0.f;
+            v[i].z = (c0 + c < C && s + 2 < S) ? src[2] : 0.f;
+            v[i].w = (c0 + c < C && s + 3 < S) ? src[3] : 0.f;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        float* d = &tile[t / 16 + 16 * i][4 * (t % 16)];
+        d[0] = v[i].x; d[1] = v[i].y; d[2] = v[i].z; d[3] = v[i].w;
     }
     __syncthreads();
     const int64_t plane = (int64_t)B * S * C_pad;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int sl = ty + 8 * i;
+    for (int i = 0; i < 2; ++i) {
+        const int c4 = t % 8, sl = t / 8 + 32 * i;
         const int64_t s = s0 + sl;
         if (s >= S) continue;
-        float hi, lo;
-        split_tf32(tile[tx][sl], hi, lo);
-        const int64_t o = (b * S + s) * C_pad + c0 + tx;
-        xc[o] = hi;
-        xc[plane + o] = lo;
+        float4 hi, lo;
+        split_tf32(tile[4 * c4 + 0][sl], hi.x, lo.x);
+        split_tf32(tile[4 * c4 + 1][sl], hi.y, lo.y);
+        split_tf32(tile[4 * c4 + 2][sl], hi.z, lo.z);
+        split_tf32(tile[4 * c4 + 3][sl], hi.w, lo.w);
+        const int64_t o = (b * S + s) * C_pad + c0 + 4 * c4;
+        *reinterpret_cast<float4*>(xc + o) = hi;
+        *reinterpret_cast<float4*>(xc + plane + o) = lo;
+    }
+}
+
+// One launch prepares both GEMM operands: blocks [0, n_xb) move X'' tiles
+// (s-tile fastest, then c-tile, then batch), the remaining blocks W'' tiles.
+struct Tc32Prep {
+    const float* x; float* xc; const float* w; float* wp;
+    int C, C_pad, B, C_out, taps, N_pad;
+    int64_t S;
+    int n_st, n_ct, n_jt;  // x tiles along s and c; weight tiles along j
+    int64_t n_xb;
+    bool vec;
+};
+
+__global__ void __launch_bounds__(256) tc32_prepare(const __grid_constant__ Tc32Prep Q) {
+    const int64_t bid = blockIdx.x;
+    if (bid < Q.n_xb) {
+        const int64_t st = bid % Q.n_st, rest = bid / Q.n_st;
+        const int ct = (int)(rest % Q.n_ct);
+        const int64_t b = rest / Q.n_ct;
+        tc32_x_tile(Q.x, Q.xc, Q.C, Q.C_pad, Q.S, Q.B, Q.vec, st * 64, ct * 32, b);
+    } else {
+        const int64_t wb = bid - Q.n_xb;
+        const int jt = (int)(wb % Q.n_jt), ct = (int)(wb / Q.n_jt);
+        tc32_weight_tile(Q.w, Q.wp, Q.C, Q.C_out, Q.taps, Q.N_pad, Q.C_pad, ct * 32, (int64_t)jt * 64);
     }
 }
 
@@ -611,22 +657,19 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
 
     // ---- launches
     {
-        const int64_t jblk = ((int64_t)pl.N_pad * p.taps() + 255) / 256;
-        dim3 grid((unsigned)(pl.C_pad / 32), (unsigned)jblk);
-        if (jblk > 65535) return cudaErrorInvalidConfiguration;
-        tc32_weight_split<<<grid, 256, 0, stream>>>(static_cast<const float*>(w), wp, (int)p.C_in,
-                                                    (int)p.C_out, (int)p.taps(), pl.N_pad,
-                                                    pl.C_pad);
-        prof_count(prof);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    {
-        const int64_t S = p.in_spatial();
-        dim3 grid((unsigned)((S + 31) / 32), (unsigned)(pl.C_pad / 32), (unsigned)p.B);
-        if (grid.y > 65535 || grid.z > 65535 || (S + 31) / 32 >= (1ll << 31))
-            return cudaErrorInvalidConfiguration;
-        tc32_channels_last<<<grid, 256, 0, stream>>>(static_cast<const float*>(x), xc, (int)p.C_in,
-                                                     pl.C_pad, S, (int)p.B);
+        Tc32Prep Q;
+        Q.x = static_cast<const float*>(x); Q.xc = xc; Q.w = static_cast<const float*>(w); Q.wp = wp;
+        Q.C = (int)p.C_in; Q.C_pad = pl.C_pad; Q.B = (int)p.B; Q.C_out = (int)p.C_out;
+        Q.taps = (int)p.taps(); Q.N_pad = pl.N_pad;
+        Q.S = p.in_spatial();
+        Q.n_st = (int)((Q.S + 63) / 64);
+        Q.n_ct = pl.C_pad / 32;
+        Q.n_jt = (int)(((int64_t)pl.N_pad * p.taps() + 63) / 64);
+        Q.n_xb = (int64_t)Q.n_st * Q.n_ct * p.B;
+        Q.vec = (Q.S % 4) == 0 && ((uintptr_t)x % 16) == 0;
+        const int64_t blocks = Q.n_xb + (int64_t)Q.n_jt * Q.n_ct;
+        if ((Q.S + 63) / 64 >= (1ll << 31) || blocks >= (1ll << 31)) return cudaErrorInvalidConfiguration;
+        tc32_prepare<<<(unsigned)blocks, 256, 0, stream>>>(Q);
         prof_count(prof);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
