@@ -69,7 +69,7 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer + MMA + epilogue warp
 
 struct TcClass {
     int rd, rh;           // D and H residues
-    int start, count;     // tile index range
+    int count;            // tiles of this class
     int n_qd, n_qh_blk, n_qw_blk;
     int qd_ext, qh_ext;   // q extents of this class on D and H
 };
@@ -91,6 +91,7 @@ struct TcParams {
     int tap[3][kTcMaxS][kTcMaxTaps];
     int off[3][kTcMaxS][kTcMaxTaps];
     int n_classes, total_tiles;
+    int g_qd, g_qh, g_qw;   // spatial tile grid (largest over the classes)
     TcClass cls[kTcMaxClasses];
     int stages;
     uint32_t stage_bytes, a_bytes;
@@ -107,27 +108,39 @@ struct TcParams {
 
 struct Tile {
     int cls, rd, rh, b, qd, qh0, qw0, oc0;
+    bool valid;
 };
 
+// Tile order: spatial block (b, qd, qh block, qw block) outermost, then
+// (D, H) stride class, then output-channel tile, so that the tiles that read
+// the same rows of X' run at about the same time and find them in L2.  The
+// spatial grid is the largest over the classes; a class with fewer blocks on
+// an axis leaves empty slots, which every role skips alike.
 __device__ __forceinline__ Tile decode_tile(const TcParams& P, int t) {
-    const TcClass* cls = P.cls;
-    int c = 0;
-    while (c + 1 < P.n_classes && t >= cls[c + 1].start) ++c;
-    const TcClass& C = cls[c];
-    int local = t - C.start;
+    int local = t;
     Tile T;
-    T.cls = c;
+    const int oc_t = local % P.n_oc_tiles; local /= P.n_oc_tiles;
+    T.cls = local % P.n_classes; local /= P.n_classes;
+    const int qw_b = local % P.g_qw; local /= P.g_qw;
+    const int qh_b = local % P.g_qh; local /= P.g_qh;
+    T.qd = local % P.g_qd;
+    T.b = local / P.g_qd;
+    const TcClass& C = P.cls[T.cls];
     T.rd = C.rd;
     T.rh = C.rh;
-    const int oc_t = local % P.n_oc_tiles; local /= P.n_oc_tiles;
-    const int qw_b = local % C.n_qw_blk; local /= C.n_qw_blk;
-    const int qh_b = local % C.n_qh_blk; local /= C.n_qh_blk;
-    T.qd = local % C.n_qd;
-    T.b = local / C.n_qd;
+    T.valid = qw_b < C.n_qw_blk && qh_b < C.n_qh_blk && T.qd < C.n_qd;
     T.qh0 = qh_b * P.MR;
     T.qw0 = qw_b * P.WC;
     T.oc0 = oc_t * kBlockM;
     return T;
+}
+
+// The persistent CTAs take the tiles round by round (round k covers tiles
+// [k * grid, (k + 1) * grid)), each CTA one tile per round, rotated by one
+// per round: a CTA then cycles through the stride classes instead of always
+// landing on the same one when the grid is a multiple of their period.
+__device__ __forceinline__ int tile_at(int k) {
+    return k * (int)gridDim.x + (int)((blockIdx.x + (unsigned)k) % gridDim.x);
 }
 
 template <int SW>
@@ -234,8 +247,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
         uint32_t phase = 0;
         uint32_t issued = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+        for (int k = 0; (int64_t)k * gridDim.x < P.total_tiles && ok; ++k) {
+            const int t = tile_at(k);
+            if (t >= P.total_tiles) continue;
             const Tile tl = decode_tile(P, t);
+            if (!tl.valid) continue;
             for (int step = 0; step < SW && ok; ++step) {
                 const int rw = phase_of<SW>(P, tl, step);
                 const int nd_ = P.ntap[0][tl.rd], nh_ = P.ntap[1][tl.rh], nw_ = P.ntap[2][rw];
@@ -285,8 +301,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
             int stage = 0;
             uint32_t phase = 0, work_iter = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+            for (int k = 0; (int64_t)k * gridDim.x < P.total_tiles && ok; ++k) {
+                const int t = tile_at(k);
+                if (t >= P.total_tiles) continue;
                 const Tile tl = decode_tile(P, t);
+                if (!tl.valid) continue;
                 if (!tile_has_work<SW>(P, tl)) continue;
                 for (int step = 0; step < SW && ok; ++step) {
                     const int rw = phase_of<SW>(P, tl, step);
@@ -340,8 +359,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
         T* __restrict__ y = static_cast<T*>(P.y);
         uint32_t work_iter = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+        for (int k = 0; (int64_t)k * gridDim.x < P.total_tiles && ok; ++k) {
+            const int t = tile_at(k);
+            if (t >= P.total_tiles) continue;
             const Tile Tl = decode_tile(P, t);
+            if (!Tl.valid) continue;
             const TcClass& C = P.cls[Tl.cls];
             const bool work = tile_has_work<SW>(P, Tl);
             const int oc = Tl.oc0 + q * 32 + lane;
@@ -728,7 +750,7 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
     P.tma_store = P.vec_store && pl.epi_bytes > 0;
     P.epi_off = (uint32_t)(pl.stages * pl.stage_bytes);
 
-    // ---- tile classes, heaviest first (longest-processing-time order)
+    // ---- tile classes, heaviest first within each spatial block
     TcClass hc[kTcMaxClasses];
     int work[kTcMaxClasses];
     int n = 0;
@@ -760,14 +782,19 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
                 std::swap(work[i], work[j]);
                 std::swap(hc[i], hc[j]);
             }
-    int64_t total = 0;
+    int g_qd = 1, g_qh = 1, g_qw = 1;
     for (int i = 0; i < n; ++i) {
-        hc[i].start = (int)total;
-        total += hc[i].count;
+        g_qd = std::max(g_qd, hc[i].n_qd);
+        g_qh = std::max(g_qh, hc[i].n_qh_blk);
+        g_qw = std::max(g_qw, hc[i].n_qw_blk);
     }
+    const int64_t total = p.B * (int64_t)g_qd * g_qh * g_qw * std::max(n, 1) * pl.n_oc_tiles;
     if (total >= (1ll << 31)) return cudaErrorInvalidValue;
     P.n_classes = n;
-    P.total_tiles = (int)total;
+    P.total_tiles = n > 0 ? (int)total : 0;
+    P.g_qd = g_qd;
+    P.g_qh = g_qh;
+    P.g_qw = g_qw;
     for (int i = 0; i < n; ++i) P.cls[i] = hc[i];
 
     // ---- tensor maps

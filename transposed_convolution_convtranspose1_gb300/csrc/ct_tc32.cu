@@ -78,7 +78,7 @@ constexpr uint32_t kPlaneA = kBlockM * kBlockK * 4;  // one A plane of a stage (
 
 struct Tc32Class {
     int rd, rh, rw;         // residues on D, H, W
-    int start, count;       // tile index range
+    int count;              // tiles of this phase
     int n_qd, n_qh_blk, n_qw_blk;
     int qd_ext, qh_ext, qw_ext;
     int taps;               // taps of this phase (product over the axes)
@@ -98,6 +98,7 @@ struct Tc32Params {
     int tap[3][kMaxS][kMaxTaps];
     int off[3][kMaxS][kMaxTaps];
     int n_classes, total_tiles;
+    int g_qd, g_qh, g_qw;   // spatial tile grid (largest over the phases)
     Tc32Class cls[kMaxClasses];
     int stages;
     uint32_t stage_bytes;
@@ -108,24 +109,38 @@ struct Tc32Params {
 
 struct Tile {
     int cls, b, qd, qh0, qw0, oc0;
+    bool valid;
 };
 
+// Tile order: spatial block (b, qd, qh block, qw block) outermost, then stride
+// phase, then output-channel tile, so that the tiles that read the same rows
+// of X'' (every phase's taps shift the same block by a few positions) run at
+// about the same time and find them in L2.  The spatial grid is the largest
+// over the phases; a phase with fewer blocks on an axis leaves empty slots,
+// which every role skips alike.
 __device__ __forceinline__ Tile decode_tile(const Tc32Params& P, int t) {
-    int c = 0;
-    while (c + 1 < P.n_classes && t >= P.cls[c + 1].start) ++c;
-    const Tc32Class& C = P.cls[c];
-    int local = t - C.start;
+    int local = t;
     Tile T;
-    T.cls = c;
     const int oc_t = local % P.n_oc_tiles; local /= P.n_oc_tiles;
-    const int qw_b = local % C.n_qw_blk; local /= C.n_qw_blk;
-    const int qh_b = local % C.n_qh_blk; local /= C.n_qh_blk;
-    T.qd = local % C.n_qd;
-    T.b = local / C.n_qd;
+    T.cls = local % P.n_classes; local /= P.n_classes;
+    const int qw_b = local % P.g_qw; local /= P.g_qw;
+    const int qh_b = local % P.g_qh; local /= P.g_qh;
+    T.qd = local % P.g_qd;
+    T.b = local / P.g_qd;
+    const Tc32Class& C = P.cls[T.cls];
+    T.valid = qw_b < C.n_qw_blk && qh_b < C.n_qh_blk && T.qd < C.n_qd;
     T.qh0 = qh_b * P.MR;
     T.qw0 = qw_b * P.WC;
     T.oc0 = oc_t * kBlockM;
     return T;
+}
+
+// The persistent CTAs take the tiles round by round (round k covers tiles
+// [k * grid, (k + 1) * grid)), each CTA one tile per round, rotated by one
+// per round: a CTA then cycles through the stride classes instead of always
+// landing on the same one when the grid is a multiple of their period.
+__device__ __forceinline__ int tile_at(int k) {
+    return k * (int)gridDim.x + (int)((blockIdx.x + (unsigned)k) % gridDim.x);
 }
 
 // ---------------------------------------------------------------------------
@@ -181,8 +196,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
         uint32_t phase = 0;
         uint32_t issued = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+        for (int k = 0; (int64_t)k * gridDim.x < P.total_tiles && ok; ++k) {
+            const int t = tile_at(k);
+            if (t >= P.total_tiles) continue;
             const Tile tl = decode_tile(P, t);
+            if (!tl.valid) continue;
             const Tc32Class& C = P.cls[tl.cls];
             const int nd_ = P.ntap[0][C.rd], nh_ = P.ntap[1][C.rh], nw_ = P.ntap[2][C.rw];
             for (int jd = 0; jd < nd_ && ok; ++jd)
@@ -233,8 +251,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
             int stage = 0;
             uint32_t phase = 0, chunk_iter = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+            for (int k = 0; (int64_t)k * gridDim.x < P.total_tiles && ok; ++k) {
+                const int t = tile_at(k);
+                if (t >= P.total_tiles) continue;
                 const Tile tl = decode_tile(P, t);
+                if (!tl.valid) continue;
                 const Tc32Class& C = P.cls[tl.cls];
                 const int nk = C.taps * P.n_kblk;
                 for (int k0 = 0; k0 < nk && ok; k0 += kChunkKB) {
@@ -295,8 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
                      (warp - 2) * 32 * 32;
         uint32_t chunk_iter = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+        for (int k = 0; (int64_t)k * gridDim.x < P.total_tiles && ok; ++k) {
+            const int t = tile_at(k);
+            if (t >= P.total_tiles) continue;
             const Tile tl = decode_tile(P, t);
+            if (!tl.valid) continue;
             const Tc32Class& C = P.cls[tl.cls];
             const int nk = C.taps * P.n_kblk;
             const int od = C.rd + P.S[0] * tl.qd;
@@ -589,7 +613,7 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
               | ((uint32_t)(kBlockM >> 4) << 24);    // M = output channels
     P.epi_off = (uint32_t)(pl.stages * pl.stage_bytes);
 
-    // ---- tile classes (one per stride phase), heaviest first
+    // ---- tile classes (one per stride phase), heaviest first within each spatial block
     Tc32Class hc[kMaxClasses];
     int n = 0;
     for (int rd = 0; rd < p.S[0]; ++rd)
@@ -616,14 +640,19 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
                 hc[n++] = c;
             }
     std::stable_sort(hc, hc + n, [](const Tc32Class& a, const Tc32Class& b) { return a.taps > b.taps; });
-    int64_t total = 0;
+    int g_qd = 1, g_qh = 1, g_qw = 1;
     for (int i = 0; i < n; ++i) {
-        hc[i].start = (int)total;
-        total += hc[i].count;
+        g_qd = std::max(g_qd, hc[i].n_qd);
+        g_qh = std::max(g_qh, hc[i].n_qh_blk);
+        g_qw = std::max(g_qw, hc[i].n_qw_blk);
     }
+    const int64_t total = p.B * (int64_t)g_qd * g_qh * g_qw * std::max(n, 1) * pl.n_oc_tiles;
     if (total >= (1ll << 31)) return cudaErrorInvalidValue;
     P.n_classes = n;
-    P.total_tiles = (int)total;
+    P.total_tiles = n > 0 ? (int)total : 0;
+    P.g_qd = g_qd;
+    P.g_qh = g_qh;
+    P.g_qw = g_qw;
     for (int i = 0; i < n; ++i) P.cls[i] = hc[i];
 
     // ---- tensor maps
