@@ -617,31 +617,33 @@ __device__ __forceinline__ void tc_x_tile(const T* __restrict__ x, T* __restrict
     }
 }
 
-// One launch prepares both GEMM operands: blocks [0, n_xb) move X' tiles
-// (s-tile fastest, then c-tile, then batch), the remaining blocks W' tiles.
+// One launch prepares both GEMM operands: blocks [0, n_wb) move W' tiles
+// (first, so that they overlap the x tiles), the remaining blocks X' tiles
+// (s-tile fastest, then c-tile, then batch).
 struct TcPrep {
     const void* x; void* xc; const void* w; void* wp;
     int C, C_pad, B, C_out, taps, N_pad;
     int64_t S;
     int n_st, n_ct, n_jt;  // x tiles along s and c; weight tiles along j
-    int64_t n_xb;
+    int64_t n_wb;          // weight tiles (first blocks of the grid)
     bool vec;
 };
 
 template <typename T>
 __global__ void __launch_bounds__(256) tc_prepare(const __grid_constant__ TcPrep Q) {
     const int64_t bid = blockIdx.x;
-    if (bid < Q.n_xb) {
-        const int64_t st = bid % Q.n_st, rest = bid / Q.n_st;
+    if (bid < Q.n_wb) {
+        const int64_t wb = bid;
+        const int jt = (int)(wb % Q.n_jt), ct = (int)(wb / Q.n_jt);
+        tc_weight_tile<T>(static_cast<const T*>(Q.w), static_cast<T*>(Q.wp), Q.C, Q.C_out, Q.taps,
+                          Q.N_pad, Q.C_pad, ct * 64, (int64_t)jt * 64);
+    } else {
+        const int64_t xb = bid - Q.n_wb;
+        const int64_t st = xb % Q.n_st, rest = xb / Q.n_st;
         const int ct = (int)(rest % Q.n_ct);
         const int64_t b = rest / Q.n_ct;
         tc_x_tile<T>(static_cast<const T*>(Q.x), static_cast<T*>(Q.xc), Q.C, Q.C_pad, Q.S, Q.vec,
                      st * 64, ct * 64, b);
-    } else {
-        const int64_t wb = bid - Q.n_xb;
-        const int jt = (int)(wb % Q.n_jt), ct = (int)(wb / Q.n_jt);
-        tc_weight_tile<T>(static_cast<const T*>(Q.w), static_cast<T*>(Q.wp), Q.C, Q.C_out, Q.taps,
-                          Q.N_pad, Q.C_pad, ct * 64, (int64_t)jt * 64);
     }
 }
 
@@ -852,10 +854,10 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
         Q.n_st = (int)((Q.S + 63) / 64);
         Q.n_ct = pl.C_pad / 64;
         Q.n_jt = (int)(((int64_t)pl.N_pad * p.taps() + 63) / 64);
-        Q.n_xb = (int64_t)Q.n_st * Q.n_ct * p.B;
+        Q.n_wb = (int64_t)Q.n_jt * Q.n_ct;
         // 16-byte loads need S % 8 == 0 and a 16-byte aligned x
         Q.vec = (Q.S % 8) == 0 && ((uintptr_t)x % 16) == 0;
-        const int64_t blocks = Q.n_xb + (int64_t)Q.n_jt * Q.n_ct;
+        const int64_t blocks = Q.n_wb + (int64_t)Q.n_st * Q.n_ct * p.B;
         if ((Q.S + 63) / 64 >= (1ll << 31) || blocks >= (1ll << 31)) return cudaErrorInvalidConfiguration;
         tc_prepare<T><<<(unsigned)blocks, 256, 0, stream>>>(Q);
         prof_count(prof);

@@ -501,28 +501,30 @@ __device__ __forceinline__ void tc32_x_tile(const float* __restrict__ x, float* 
     }
 }
 
-// One launch prepares both GEMM operands: blocks [0, n_xb) move X'' tiles
-// (s-tile fastest, then c-tile, then batch), the remaining blocks W'' tiles.
+// One launch prepares both GEMM operands: blocks [0, n_wb) move W'' tiles
+// (first, so that they overlap the x tiles), the remaining blocks X'' tiles
+// (s-tile fastest, then c-tile, then batch).
 struct Tc32Prep {
     const float* x; float* xc; const float* w; float* wp;
     int C, C_pad, B, C_out, taps, N_pad;
     int64_t S;
     int n_st, n_ct, n_jt;  // x tiles along s and c; weight tiles along j
-    int64_t n_xb;
+    int64_t n_wb;          // weight tiles (first blocks of the grid)
     bool vec;
 };
 
 __global__ void __launch_bounds__(256) tc32_prepare(const __grid_constant__ Tc32Prep Q) {
     const int64_t bid = blockIdx.x;
-    if (bid < Q.n_xb) {
-        const int64_t st = bid % Q.n_st, rest = bid / Q.n_st;
+    if (bid < Q.n_wb) {
+        const int64_t wb = bid;
+        const int jt = (int)(wb % Q.n_jt), ct = (int)(wb / Q.n_jt);
+        tc32_weight_tile(Q.w, Q.wp, Q.C, Q.C_out, Q.taps, Q.N_pad, Q.C_pad, ct * 32, (int64_t)jt * 64);
+    } else {
+        const int64_t xb = bid - Q.n_wb;
+        const int64_t st = xb % Q.n_st, rest = xb / Q.n_st;
         const int ct = (int)(rest % Q.n_ct);
         const int64_t b = rest / Q.n_ct;
         tc32_x_tile(Q.x, Q.xc, Q.C, Q.C_pad, Q.S, Q.B, Q.vec, st * 64, ct * 32, b);
-    } else {
-        const int64_t wb = bid - Q.n_xb;
-        const int jt = (int)(wb % Q.n_jt), ct = (int)(wb / Q.n_jt);
-        tc32_weight_tile(Q.w, Q.wp, Q.C, Q.C_out, Q.taps, Q.N_pad, Q.C_pad, ct * 32, (int64_t)jt * 64);
     }
 }
 
@@ -694,9 +696,9 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
         Q.n_st = (int)((Q.S + 63) / 64);
         Q.n_ct = pl.C_pad / 32;
         Q.n_jt = (int)(((int64_t)pl.N_pad * p.taps() + 63) / 64);
-        Q.n_xb = (int64_t)Q.n_st * Q.n_ct * p.B;
+        Q.n_wb = (int64_t)Q.n_jt * Q.n_ct;
         Q.vec = (Q.S % 4) == 0 && ((uintptr_t)x % 16) == 0;
-        const int64_t blocks = Q.n_xb + (int64_t)Q.n_jt * Q.n_ct;
+        const int64_t blocks = Q.n_wb + (int64_t)Q.n_st * Q.n_ct * p.B;
         if ((Q.S + 63) / 64 >= (1ll << 31) || blocks >= (1ll << 31)) return cudaErrorInvalidConfiguration;
         tc32_prepare<<<(unsigned)blocks, 256, 0, stream>>>(Q);
         prof_count(prof);
