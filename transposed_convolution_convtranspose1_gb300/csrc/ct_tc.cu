@@ -239,6 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = tmem_base_slot;
+    // X' and W' come from the preceding prepare kernel (launched as its
+    // programmatic dependent): wait for its writes before any operand load.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -631,6 +634,8 @@ struct TcPrep {
 
 template <typename T>
 __global__ void __launch_bounds__(256) tc_prepare(const __grid_constant__ TcPrep Q) {
+    // the GEMM that follows may begin its prologue now
+    asm volatile("griddepcontrol.launch_dependents;");
     const int64_t bid = blockIdx.x;
     if (bid < Q.n_wb) {
         const int64_t wb = bid;
@@ -698,8 +703,20 @@ cudaError_t launch_gemm(const TcParams& P, int grid, size_t smem, cudaStream_t s
     cudaError_t e = cudaFuncSetAttribute(tc_phase_gemm<T, SW>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    tc_phase_gemm<T, SW><<<grid, kThreads, smem, stream>>>(P);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the GEMM's CTAs may start (barrier
+    // init, TMEM allocation, tensor-map prefetch) while the prepare kernel
+    // finishes; they wait for its results before the first operand load.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_phase_gemm<T, SW>, P);
 }
 
 template <typename T>

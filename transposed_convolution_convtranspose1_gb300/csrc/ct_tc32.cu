@@ -189,6 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = tmem_base_slot;
+    // X'' and W'' come from the preceding prepare kernel (launched as its
+    // programmatic dependent): wait for its writes before any operand load.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -514,6 +517,8 @@ struct Tc32Prep {
 };
 
 __global__ void __launch_bounds__(256) tc32_prepare(const __grid_constant__ Tc32Prep Q) {
+    // the GEMM that follows may begin its prologue now
+    asm volatile("griddepcontrol.launch_dependents;");
     const int64_t bid = blockIdx.x;
     if (bid < Q.n_wb) {
         const int64_t wb = bid;
@@ -709,8 +714,23 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
     e = cudaFuncSetAttribute(tc32_phase_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     prof_begin(prof, stream);
-    tc32_phase_gemm<<<grid, kThreads, smem, stream>>>(P);
-    e = cudaGetLastError();
+    {
+        // Programmatic dependent launch: the GEMM's CTAs may start (barrier
+        // init, TMEM allocation, tensor-map prefetch) while the prepare
+        // kernel finishes; they wait for its results before the first
+        // operand load.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, tc32_phase_gemm, P);
+    }
     prof_end(prof, stream);
     prof_count(prof);
     return e;
