@@ -98,17 +98,20 @@ struct Tc32Params {
     int tap[3][kMaxS][kMaxTaps];
     int off[3][kMaxS][kMaxTaps];
     int n_classes, total_tiles;
+    int n_full, total_slots;  // tiles run whole; work slots (the rest run as two halves)
     int g_qd, g_qh, g_qw;   // spatial tile grid (largest over the phases)
     Tc32Class cls[kMaxClasses];
     int stages;
     uint32_t stage_bytes;
-    uint32_t idesc;
+    uint32_t idesc;         // N = kNP positions
+    uint32_t idesc_half;    // N = kNP / 2 (half tiles)
     uint32_t tmem_cols;
     uint32_t epi_off;       // offset of the epilogue blocks from the ring
 };
 
 struct Tile {
     int cls, b, qd, qh0, qw0, oc0;
+    int half;   // -1: the whole tile; 0 / 1: its first / second half of positions
     bool valid;
 };
 
@@ -132,6 +135,24 @@ __device__ __forceinline__ Tile decode_tile(const Tc32Params& P, int t) {
     T.qh0 = qh_b * P.MR;
     T.qw0 = qw_b * P.WC;
     T.oc0 = oc_t * kBlockM;
+    T.half = -1;
+    return T;
+}
+
+// Work slot s: slots below n_full are whole tiles; the tiles after them (the
+// last, partial round of a whole-tile schedule) run as two halves of kNP / 2
+// positions each, so that the last round takes half as long.  A half tile
+// shifts the tile's origin by half its rows (or half its width when it is
+// one row) and uses the first kNP / 2 positions of the box loaded there.
+__device__ __forceinline__ Tile decode_slot(const Tc32Params& P, int s) {
+    if (s < P.n_full) return decode_tile(P, s);
+    const int hs = s - P.n_full;
+    Tile T = decode_tile(P, P.n_full + hs / 2);
+    T.half = hs & 1;
+    if (P.MR >= 2) T.qh0 += T.half * (P.MR / 2);
+    else T.qw0 += T.half * (P.WC / 2);
+    const Tc32Class& C = P.cls[T.cls];
+    T.valid = T.valid && T.qh0 < C.qh_ext && T.qw0 < C.qw_ext;
     return T;
 }
 
@@ -199,10 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
         uint32_t phase = 0;
         uint32_t issued = 0;
         bool ok = true;
-        for (int k = 0; (int64_t)k * gridDim.x < P.total_tiles && ok; ++k) {
+        for (int k = 0; (int64_t)k * gridDim.x < P.total_slots && ok; ++k) {
             const int t = tile_at(k);
-            if (t >= P.total_tiles) continue;
-            const Tile tl = decode_tile(P, t);
+            if (t >= P.total_slots) continue;
+            const Tile tl = decode_slot(P, t);
             if (!tl.valid) continue;
             const Tc32Class& C = P.cls[tl.cls];
             const int nd_ = P.ntap[0][C.rd], nh_ = P.ntap[1][C.rh], nw_ = P.ntap[2][C.rw];
@@ -254,10 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
             int stage = 0;
             uint32_t phase = 0, chunk_iter = 0;
             bool ok = true;
-            for (int k = 0; (int64_t)k * gridDim.x < P.total_tiles && ok; ++k) {
+            for (int k = 0; (int64_t)k * gridDim.x < P.total_slots && ok; ++k) {
                 const int t = tile_at(k);
-                if (t >= P.total_tiles) continue;
-                const Tile tl = decode_tile(P, t);
+                if (t >= P.total_slots) continue;
+                const Tile tl = decode_slot(P, t);
                 if (!tl.valid) continue;
                 const Tc32Class& C = P.cls[tl.cls];
                 const int nk = C.taps * P.n_kblk;
@@ -271,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
                     }
                     tc_fence_after();
                     const uint32_t d = tmem_base + slot * kNP;
+                    const uint32_t idesc = tl.half < 0 ? P.idesc : P.idesc_half;
                     const int k1 = min(nk, k0 + kChunkKB);
                     for (int j = k0; j < k1; ++j) {
                         if (!mbar_wait(smem_u32(&full_bar[stage]), phase, kErrMma, &abort_flag)) {
@@ -286,9 +308,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
                         for (int k = 0; k < kBlockK / 8; ++k) {
                             // K-step of 8 TF32 elements = 32 bytes (encoded >> 4: 2)
                             const uint64_t o = 2 * k;
-                            mma_tf32(d, al + o, bh + o, P.idesc, (j > k0 || k > 0) ? 1u : 0u);
-                            mma_tf32(d, ah + o, bl + o, P.idesc, 1u);
-                            mma_tf32(d, ah + o, bh + o, P.idesc, 1u);
+                            mma_tf32(d, al + o, bh + o, idesc, (j > k0 || k > 0) ? 1u : 0u);
+                            mma_tf32(d, ah + o, bl + o, idesc, 1u);
+                            mma_tf32(d, ah + o, bh + o, idesc, 1u);
                         }
                         mma_commit(smem_u32(&empty_bar[stage]));
                         if (++stage == P.stages) {
@@ -319,15 +341,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
                      (warp - 2) * 32 * 32;
         uint32_t chunk_iter = 0;
         bool ok = true;
-        for (int k = 0; (int64_t)k * gridDim.x < P.total_tiles && ok; ++k) {
+        for (int k = 0; (int64_t)k * gridDim.x < P.total_slots && ok; ++k) {
             const int t = tile_at(k);
-            if (t >= P.total_tiles) continue;
-            const Tile tl = decode_tile(P, t);
+            if (t >= P.total_slots) continue;
+            const Tile tl = decode_slot(P, t);
             if (!tl.valid) continue;
             const Tc32Class& C = P.cls[tl.cls];
             const int nk = C.taps * P.n_kblk;
             const int od = C.rd + P.S[0] * tl.qd;
             const bool d_ok = tl.qd < C.qd_ext;
+            // a half tile has positions [0, kNP / 2) only: the h = 1 warps keep
+            // the chunk handshakes and store nothing
+            const bool idle = tl.half >= 0 && h == 1;
             // column group c (32 positions) of this warp lies in one output row
             auto group_valid = [&](int c, int& qh, int& qwb) {
                 const int p0 = h * kEpiCols + c * 32;
@@ -348,19 +373,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
                 const uint32_t col0 = tmem_base + ((uint32_t)(q * 32) << 16) + slot * kNP + h * kEpiCols;
                 // every column is read (columns past the output only feed
                 // sums that are never stored); 16 per load keeps acc in registers
+                if (!idle) {
 #pragma unroll
-                for (int c = 0; c < kEpiCols / 16; ++c) {
-                    float v[16];
-                    tmem_ld16(col0 + c * 16, v);
-                    tmem_ld_wait();
+                    for (int c = 0; c < kEpiCols / 16; ++c) {
+                        float v[16];
+                        tmem_ld16(col0 + c * 16, v);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[c * 16 + i] += v[i];
+                        for (int i = 0; i < 16; ++i) acc[c * 16 + i] += v[i];
+                    }
                 }
                 tc_fence_before();
                 mbar_arrive(smem_u32(&sempty_bar[slot]));
                 ++chunk_iter;
             }
             if (!ok) break;
+            if (idle) continue;
             const int oc_lane = tl.oc0 + q * 32 + lane;
             const float bv = (P.bias != nullptr && oc_lane < P.C_out) ? P.bias[oc_lane] : 0.f;
             const int64_t plane = (int64_t)P.O[0] * P.O[1];
@@ -618,6 +646,7 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
               | (2u << 10)                           // B = tf32
               | ((uint32_t)(kNP >> 3) << 17)         // N = positions
               | ((uint32_t)(kBlockM >> 4) << 24);    // M = output channels
+    P.idesc_half = (P.idesc & ~(0x3Fu << 17)) | ((uint32_t)((kNP / 2) >> 3) << 17);
     P.epi_off = (uint32_t)(pl.stages * pl.stage_bytes);
 
     // ---- tile classes (one per stride phase), heaviest first within each spatial block
@@ -657,6 +686,15 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
     if (total >= (1ll << 31)) return cudaErrorInvalidValue;
     P.n_classes = n;
     P.total_tiles = n > 0 ? (int)total : 0;
+    {
+        // tiles of a last, partial round run as halves when they then fit in
+        // one round of the grid
+        const int64_t G = dev.sm_count;
+        const int64_t rem = P.total_tiles % G;
+        const int64_t R = (rem != 0 && 2 * rem <= G) ? rem : 0;
+        P.n_full = (int)(P.total_tiles - R);
+        P.total_slots = (int)(P.total_tiles + R);
+    }
     P.g_qd = g_qd;
     P.g_qh = g_qh;
     P.g_qw = g_qw;
@@ -710,7 +748,7 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     const size_t smem = (size_t)P.stages * P.stage_bytes + pl.epi_bytes + 1024;
-    const int grid = std::max(1, std::min(P.total_tiles, dev.sm_count));
+    const int grid = std::max(1, std::min(P.total_slots, dev.sm_count));
     e = cudaFuncSetAttribute(tc32_phase_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     prof_begin(prof, stream);
