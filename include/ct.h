@@ -226,10 +226,17 @@ int ct_conv_transpose_route_workspace_bytes(int nd, int64_t B, int64_t C_in,
 
 /*
  * End-to-end call on HOST buffers: x, w, bias (nullable) and y are host
- * pointers (pinned memory gives the fastest copies).  The call allocates
- * device buffers stream-ordered, copies the inputs to the device, runs
- * ct_conv_transpose_nd, copies y back, frees the buffers and synchronises
- * `stream` before returning.  Same validation and errors as the device call.
+ * pointers (pinned memory gives the fastest copies).  The call takes device
+ * buffers from a library-owned stream-ordered memory pool (one per device,
+ * created by the first call; it keeps its memory between calls until
+ * ct_host_buffers_release), copies w and bias in, then runs the batch in up
+ * to 8 chunks as a pipeline: chunk c's input copy (on a library side stream),
+ * its computation (on `stream`, as ct_conv_transpose_nd) and its output copy
+ * (on a second side stream) overlap the neighbouring chunks' copies.  Calls
+ * whose x and y together hold less than 8 MiB, or with B = 1, run as one
+ * chunk.  The call synchronises `stream` before returning; concurrent calls
+ * from several host threads on one device are serialised.  Same validation
+ * and errors as the device call.
  */
 int ct_conv_transpose_nd_host(const void* x, const void* w, const void* bias,
                               void* y, int nd, int64_t B, int64_t C_in,
@@ -238,6 +245,13 @@ int ct_conv_transpose_nd_host(const void* x, const void* w, const void* bias,
                               const int* pad_lo, const int* pad_hi,
                               const int* dilation, const int* output_padding,
                               int groups, int dtype, void* stream);
+
+/*
+ * Returns the memory the host-buffer entry point keeps in its pool on the
+ * current device to the device (the pool itself stays, empty).  The memory
+ * is otherwise kept until process exit.  Host only; CT_ERR_CUDA on failure.
+ */
+int ct_host_buffers_release(void);
 
 /*
  * Size of the fixed scratch array behind ct_conv_transpose_nd_noalloc.

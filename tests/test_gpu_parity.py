@@ -238,7 +238,7 @@ def test_side_stream_and_explicit_workspace():
         assert e.value.status == ct.ct.CT_ERR_WORKSPACE
 
 
-@pytest.mark.parametrize("i", [0, 3])
+@pytest.mark.parametrize("i", [0, 1, 2, 3])
 def test_host_entry_point_matches_device(i):
     p = synth.workload(i)
     x, w, b = synth.make_inputs(p)
@@ -251,3 +251,26 @@ def test_host_entry_point_matches_device(i):
     yd = run(p, x, w, b)
     torch.cuda.synchronize()
     assert torch.equal(yh, yd.cpu())
+
+
+def test_host_entry_point_pipeline_chunks_stream_and_release():
+    """B = 11 runs as 6 batch chunks of 2 (the last of 1) through the copy /
+    compute / copy pipeline; the result equals the device call's bit for bit,
+    on the default stream and on a caller's stream, before and after the
+    library's pool memory is released."""
+    p = synth.problem("host_chunks", 11, 48, 40, (3000,), 8, stride=4, pad=2, seed=901)
+    x, w, b = synth.make_inputs(p)
+    O = ct.ct_conv_transpose_out_shape(p.spatial, p.k, p.stride, p.pad_lo, p.pad_hi,
+                                       p.dilation, p.output_padding)
+    hx, hw, hb = x.pin_memory(), w.pin_memory(), b.pin_memory()
+    yd = run(p, x, w, b)
+    torch.cuda.synchronize()
+    ref = yd.cpu()
+    s = torch.cuda.Stream()
+    for stream in (None, s, None):
+        yh = torch.full((p.B, p.C_out) + O, float("nan"), dtype=p.torch_dtype).pin_memory()
+        ct.ct_conv_transpose_nd_host(hx, hw, hb, yh, p.stride, p.pad_lo, p.pad_hi, p.dilation,
+                                     p.output_padding, p.groups, stream=stream)
+        assert torch.equal(yh, ref)
+        ct.ct_host_buffers_release()
+

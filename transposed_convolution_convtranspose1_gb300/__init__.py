@@ -12,4 +12,5 @@ from .ct import (  # noqa: F401
     ROUTE_NAMES, CtError, conv_transpose, ct_conv_transpose_nd, ct_conv_transpose_nd_host, ct_conv_transpose_nd_profiled,
     ct_conv_transpose_nd_noalloc, CT_NOALLOC_SCRATCH_BYTES,
     ct_conv_transpose_out_shape, ct_conv_transpose_route, ct_conv_transpose_workspace_bytes,
-    ct_device_status, ct_last_error, ct_status_string, ct_version, dtype_code, lib)
+    ct_device_status, ct_host_buffers_release, ct_last_error, ct_status_string, ct_version,
+    dtype_code, lib)

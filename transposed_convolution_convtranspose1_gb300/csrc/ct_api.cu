@@ -178,6 +178,58 @@ int run(const Problem& p, int route, const void* x, const void* w, const void* b
     return CT_OK;
 }
 
+// Resources of the host-buffer entry point, one set per device, created on
+// first use and kept until process exit: a stream-ordered memory pool that
+// keeps its memory between calls (no re-mapping per call; returned by
+// ct_host_buffers_release), two non-blocking side streams (input and output
+// copies) and the events that order the pipeline.
+constexpr size_t kHostPipelineMinBytes = 8u << 20;  // smaller calls run as one chunk
+constexpr int kHostMaxChunks = 8;
+
+struct HostRes {
+    std::mutex mu;
+    cudaMemPool_t pool = nullptr;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev_start = nullptr, ev_done_in = nullptr, ev_done_out = nullptr;
+    cudaEvent_t ev_in[kHostMaxChunks] = {}, ev_comp[kHostMaxChunks] = {};
+};
+
+cudaError_t host_resources(HostRes** out) {
+    static std::mutex mu;
+    static HostRes* res[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (res[dev]) {
+        *out = res[dev];
+        return cudaSuccess;
+    }
+    HostRes* R = new HostRes();
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    e = cudaMemPoolCreate(&R->pool, &props);
+    if (e == cudaSuccess) {
+        uint64_t keep = UINT64_MAX;
+        e = cudaMemPoolSetAttribute(R->pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    }
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&R->s_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&R->s_out, cudaStreamNonBlocking);
+    cudaEvent_t* evs[3] = {&R->ev_start, &R->ev_done_in, &R->ev_done_out};
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(evs[i], cudaEventDisableTiming);
+    for (int i = 0; i < kHostMaxChunks && e == cudaSuccess; ++i) {
+        e = cudaEventCreateWithFlags(&R->ev_in[i], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&R->ev_comp[i], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return e;  // leaks the partial set; the device is unusable anyway
+    res[dev] = R;
+    *out = R;
+    return cudaSuccess;
+}
+
 int check_pointers(const Problem& p, const void* x, const void* w, const void* bias, const void* y) {
     if (p.x_elems() > 0 && !x) return fail(CT_ERR_NULL, "x is NULL");
     if (p.w_elems() > 0 && !w) return fail(CT_ERR_NULL, "w is NULL");
@@ -389,43 +441,92 @@ int ct_conv_transpose_nd_host(const void* x, const void* w, const void* bias, vo
     if (rc != CT_OK) return rc;
     rc = check_pointers(p, x, w, bias, y);
     if (rc != CT_OK) return rc;
+    HostRes* R = nullptr;
+    cudaError_t e = host_resources(&R);
+    if (e != cudaSuccess) return cuda_fail(e, "host call resources");
+    std::lock_guard<std::mutex> lock(R->mu);  // the side streams and events are shared
     cudaStream_t s = (cudaStream_t)stream;
     const size_t eb = p.elem_bytes();
-    const size_t xb = (size_t)p.x_elems() * eb, wb = (size_t)p.w_elems() * eb;
-    const size_t bb = bias ? (size_t)p.C_out * eb : 0, yb = (size_t)p.y_elems() * eb;
+    const size_t wb = (size_t)p.w_elems() * eb;
+    const size_t bb = bias ? (size_t)p.C_out * eb : 0;
+    // batch chunks: chunk c's input copy, compute and output copy run on
+    // three streams, so that copies in both directions overlap the compute
+    const size_t xb_all = (size_t)p.x_elems() * eb, yb_all = (size_t)p.y_elems() * eb;
+    int64_t nchunk = 1;
+    if (p.B > 1 && xb_all + yb_all >= kHostPipelineMinBytes)
+        nchunk = std::min<int64_t>(p.B, kHostMaxChunks);
+    const int64_t bc = (p.B + nchunk - 1) / nchunk;  // batch elements per chunk
+    nchunk = p.B > 0 ? (p.B + bc - 1) / bc : 1;
+    const size_t xb1 = (size_t)(p.x_elems() / std::max<int64_t>(p.B, 1)) * eb;  // per batch element
+    const size_t yb1 = (size_t)(p.y_elems() / std::max<int64_t>(p.B, 1)) * eb;
+    Problem pc = p;  // the largest and the last chunk size the workspace
+    pc.B = std::min<int64_t>(bc, p.B);
+    size_t ws = route_workspace(pc, choose_route(pc));
+    pc.B = p.B - (nchunk - 1) * bc;
+    if (pc.B > 0) ws = std::max(ws, route_workspace(pc, choose_route(pc)));
     auto round = [](size_t n) { return (n + 255) / 256 * 256; };
-    const size_t ws = route_workspace(p, choose_route(p));
-    const size_t total = round(xb) + round(wb) + round(bb) + round(yb) + round(ws);
+    const size_t total = round(xb_all) + round(wb) + round(bb) + round(yb_all) + round(ws);
     char* base = nullptr;
-    cudaError_t e = cudaSuccess;
     if (total > 0) {
-        e = cudaMallocAsync((void**)&base, total, s);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(host call buffers)");
+        e = cudaMallocFromPoolAsync((void**)&base, total, R->pool, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync(host call buffers)");
     }
     char* dx = base;
-    char* dw = dx + round(xb);
+    char* dw = dx + round(xb_all);
     char* db = dw + round(wb);
     char* dy = db + round(bb);
-    char* dws = dy + round(yb);
-    if (xb) e = cudaMemcpyAsync(dx, x, xb, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess && wb) e = cudaMemcpyAsync(dw, w, wb, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess && bb) e = cudaMemcpyAsync(db, bias, bb, cudaMemcpyHostToDevice, s);
+    char* dws = dy + round(yb_all);
     rc = CT_OK;
-    if (e != cudaSuccess) {
-        rc = cuda_fail(e, "cudaMemcpyAsync(host to device)");
-    } else {
-        rc = ct_conv_transpose_nd(dx, dw, bias ? db : nullptr, dy, ws ? dws : nullptr, ws, nd, B,
-                                  C_in, C_out, in_spatial, k, stride, pad_lo, pad_hi, dilation,
-                                  output_padding, groups, dtype, stream);
-        if (rc == CT_OK && yb) {
-            e = cudaMemcpyAsync(y, dy, yb, cudaMemcpyDeviceToHost, s);
-            if (e != cudaSuccess) rc = cuda_fail(e, "cudaMemcpyAsync(device to host)");
+    // the side streams start after everything already queued on `stream`
+    e = cudaEventRecord(R->ev_start, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(R->s_in, R->ev_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(R->s_out, R->ev_start, 0);
+    if (e == cudaSuccess && wb) e = cudaMemcpyAsync(dw, w, wb, cudaMemcpyHostToDevice, R->s_in);
+    if (e == cudaSuccess && bb) e = cudaMemcpyAsync(db, bias, bb, cudaMemcpyHostToDevice, R->s_in);
+    if (e != cudaSuccess) rc = cuda_fail(e, "cudaMemcpyAsync(host to device)");
+    for (int64_t c = 0; c < nchunk && rc == CT_OK; ++c) {
+        const int64_t b0 = c * bc, nb = std::min(bc, p.B - b0);
+        const size_t xo = (size_t)b0 * xb1, yo = (size_t)b0 * yb1;
+        if (nb > 0 && xb1 > 0)
+            e = cudaMemcpyAsync(dx + xo, static_cast<const char*>(x) + xo, nb * xb1,
+                                cudaMemcpyHostToDevice, R->s_in);
+        if (e == cudaSuccess) e = cudaEventRecord(R->ev_in[c], R->s_in);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, R->ev_in[c], 0);
+        if (e != cudaSuccess) {
+            rc = cuda_fail(e, "cudaMemcpyAsync(host to device)");
+            break;
         }
+        rc = ct_conv_transpose_nd(dx + xo, dw, bias ? db : nullptr, dy + yo, ws ? dws : nullptr, ws,
+                                  nd, nb, C_in, C_out, in_spatial, k, stride, pad_lo, pad_hi,
+                                  dilation, output_padding, groups, dtype, stream);
+        if (rc != CT_OK) break;
+        e = cudaEventRecord(R->ev_comp[c], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(R->s_out, R->ev_comp[c], 0);
+        if (e == cudaSuccess && nb > 0 && yb1 > 0)
+            e = cudaMemcpyAsync(static_cast<char*>(y) + yo, dy + yo, nb * yb1, cudaMemcpyDeviceToHost,
+                                R->s_out);
+        if (e != cudaSuccess) rc = cuda_fail(e, "cudaMemcpyAsync(device to host)");
     }
+    // `stream` waits for both side streams before the buffers go back to the pool
+    cudaError_t e2 = cudaEventRecord(R->ev_done_in, R->s_in);
+    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(s, R->ev_done_in, 0);
+    if (e2 == cudaSuccess) e2 = cudaEventRecord(R->ev_done_out, R->s_out);
+    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(s, R->ev_done_out, 0);
     if (base) cudaFreeAsync(base, s);
     e = cudaStreamSynchronize(s);
+    if (rc == CT_OK && e2 != cudaSuccess) rc = cuda_fail(e2, "ordering the host call's streams");
     if (rc == CT_OK && e != cudaSuccess) rc = cuda_fail(e, "cudaStreamSynchronize");
     return rc;
+}
+
+int ct_host_buffers_release(void) {
+    HostRes* R = nullptr;
+    cudaError_t e = host_resources(&R);
+    if (e != cudaSuccess) return cuda_fail(e, "host call resources");
+    std::lock_guard<std::mutex> lock(R->mu);
+    e = cudaMemPoolTrimTo(R->pool, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolTrimTo");
+    return CT_OK;
 }
 
 }  // extern "C"

@@ -48,7 +48,7 @@ EXPORTS = ("ct_version", "ct_last_error", "ct_status_string",
            "ct_conv_transpose_route", "ct_conv_transpose_route_workspace_bytes",
            "ct_conv_transpose_nd", "ct_conv_transpose_nd_route",
            "ct_conv_transpose_nd_host", "ct_conv_transpose_nd_profiled",
-           "ct_conv_transpose_nd_noalloc", "ct_device_status")
+           "ct_conv_transpose_nd_noalloc", "ct_device_status", "ct_host_buffers_release")
 
 # Size of the static scratch behind ct_conv_transpose_nd_noalloc (CT_NOALLOC_SCRATCH_BYTES).
 CT_NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -106,6 +106,8 @@ def _declare(h):
     h.ct_conv_transpose_nd_noalloc.argtypes = [_vp, _vp, _vp, _vp] + _SHAPE_ARGS + [_vp]
     h.ct_device_status.restype = ctypes.c_int
     h.ct_device_status.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_uint)]
+    h.ct_host_buffers_release.restype = ctypes.c_int
+    h.ct_host_buffers_release.argtypes = []
 
 
 def lib():
@@ -314,6 +316,11 @@ def ct_conv_transpose_nd_noalloc(x: torch.Tensor, w: torch.Tensor, bias: Optiona
     _check(lib().ct_conv_transpose_nd_noalloc(
         _ptr(x), _ptr(w), _ptr(bias), _ptr(y),
         *_shape_args(B, C_in, C_out, ax, groups, dtype_code(x.dtype)), s))
+
+
+def ct_host_buffers_release() -> None:
+    """Return the device memory the host-buffer entry point keeps in its pool."""
+    _check(lib().ct_host_buffers_release())
 
 
 def ct_device_status(clear: bool = True):
