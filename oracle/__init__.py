@@ -1,6 +1,7 @@
-"""fp64 CPU oracle for the forward transposed convolution.
+"""fp64 CPU oracle for the forward transposed convolution and its gradients.
 
 TEST INFRASTRUCTURE ONLY: the test suite, the package smoke check and the
 CPU-baseline leg of the benchmark use it; the product never imports it.
 """
-from .oracle import build, conv_transpose, out_shape, points, to_f64  # noqa: F401
+from .oracle import (build, conv_transpose, conv_transpose_backward, out_shape, points,  # noqa: F401
+                     to_f64)

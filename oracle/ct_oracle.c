@@ -1,5 +1,6 @@
 /*
- * ct_oracle.c -- fp64 CPU oracle for the forward transposed convolution.
+ * ct_oracle.c -- fp64 CPU oracle for the forward transposed convolution and
+ * its gradients.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product (the CUDA library and its
  * Python binding) links, loads or calls this file.  Only the test suite, the
@@ -261,5 +262,179 @@ int oracle_points_f64(const double* x, const double* w, const double* bias,
         }
         out[e] = acc;
     }
+    return OR_OK;
+}
+
+/*
+ * Backward pass (gradients), in fp64: the adjoint of the scatter above, as the
+ * SKaiNET pull request's Summary describes its convTranspose2dBackward (input,
+ * weight and bias gradients).  Every product of the forward pass,
+ *     y[b, oc, o] += x[b, ic, i] * w[ic, oc_g, t]   at o_a = i_a*s_a - pad_lo_a + t_a*d_a
+ * (o inside the output, ic in oc's group), contributes
+ *     dx[b, ic, i]    += dy[b, oc, o] * w[ic, oc_g, t]
+ *     dw[ic, oc_g, t] += dy[b, oc, o] * x[b, ic, i]
+ * and every output element contributes db[oc] += dy[b, oc, o].
+ * Slices: dx by (b, ic), dw by ic, db by oc; each is one thread's at a time,
+ * with a fixed loop order, so the result does not depend on the thread count.
+ */
+typedef struct {
+    const or_problem* p;
+    const double* x;      /* [B, C_in, I...] */
+    const double* w;      /* [C_in, C_out/groups, K...] */
+    const double* dy;     /* [B, C_out, O...] */
+    double* dx;           /* [B, C_in, I...] or NULL */
+    double* dw;           /* [C_in, C_out/groups, K...] or NULL */
+    double* db;           /* [C_out] or NULL */
+    int64_t next_task;
+    pthread_mutex_t lock;
+} or_bjob;
+
+/* dx[b, ic, :]: for each oc of the group and tap t, walk the input positions
+ * and read dy at the output position the forward pass wrote them to. */
+static void or_dx_slice(const or_bjob* j, int64_t b, int64_t ic)
+{
+    const or_problem* p = j->p;
+    const int64_t Cig = p->C_in / p->groups, Cog = p->C_out / p->groups;
+    const int64_t g = ic / Cig;
+    const int64_t In = p->I[0] * p->I[1] * p->I[2];
+    const int64_t On = p->O[0] * p->O[1] * p->O[2];
+    const int64_t Kn = p->K[0] * p->K[1] * p->K[2];
+    double* dxs = j->dx + (b * p->C_in + ic) * In;
+    for (int64_t i = 0; i < In; ++i) dxs[i] = 0.0;
+    for (int64_t oc_g = 0; oc_g < Cog; ++oc_g) {
+        const int64_t oc = g * Cog + oc_g;
+        const double* dys = j->dy + (b * p->C_out + oc) * On;
+        const double* ws = j->w + (ic * Cog + oc_g) * Kn;
+        for (int64_t t0 = 0; t0 < p->K[0]; ++t0)
+        for (int64_t t1 = 0; t1 < p->K[1]; ++t1)
+        for (int64_t t2 = 0; t2 < p->K[2]; ++t2) {
+            const double wv = ws[(t0 * p->K[1] + t1) * p->K[2] + t2];
+            for (int64_t i0 = 0; i0 < p->I[0]; ++i0) {
+                const int64_t o0 = i0 * p->S[0] - p->PL[0] + t0 * p->DL[0];
+                if (o0 < 0 || o0 >= p->O[0]) continue;
+                for (int64_t i1 = 0; i1 < p->I[1]; ++i1) {
+                    const int64_t o1 = i1 * p->S[1] - p->PL[1] + t1 * p->DL[1];
+                    if (o1 < 0 || o1 >= p->O[1]) continue;
+                    double* dxr = dxs + (i0 * p->I[1] + i1) * p->I[2];
+                    const double* dyr = dys + (o0 * p->O[1] + o1) * p->O[2];
+                    for (int64_t i2 = 0; i2 < p->I[2]; ++i2) {
+                        const int64_t o2 = i2 * p->S[2] - p->PL[2] + t2 * p->DL[2];
+                        if (o2 < 0 || o2 >= p->O[2]) continue;
+                        dxr[i2] += dyr[o2] * wv;
+                    }
+                }
+            }
+        }
+    }
+}
+
+/* dw[ic, :, :]: for each oc of the group and tap t, the sum over batch and
+ * input positions of x times dy at the position the product landed on. */
+static void or_dw_slice(const or_bjob* j, int64_t ic)
+{
+    const or_problem* p = j->p;
+    const int64_t Cig = p->C_in / p->groups, Cog = p->C_out / p->groups;
+    const int64_t g = ic / Cig;
+    const int64_t In = p->I[0] * p->I[1] * p->I[2];
+    const int64_t On = p->O[0] * p->O[1] * p->O[2];
+    const int64_t Kn = p->K[0] * p->K[1] * p->K[2];
+    for (int64_t oc_g = 0; oc_g < Cog; ++oc_g) {
+        const int64_t oc = g * Cog + oc_g;
+        for (int64_t t0 = 0; t0 < p->K[0]; ++t0)
+        for (int64_t t1 = 0; t1 < p->K[1]; ++t1)
+        for (int64_t t2 = 0; t2 < p->K[2]; ++t2) {
+            double acc = 0.0;
+            for (int64_t b = 0; b < p->B; ++b) {
+                const double* xs = j->x + (b * p->C_in + ic) * In;
+                const double* dys = j->dy + (b * p->C_out + oc) * On;
+                for (int64_t i0 = 0; i0 < p->I[0]; ++i0) {
+                    const int64_t o0 = i0 * p->S[0] - p->PL[0] + t0 * p->DL[0];
+                    if (o0 < 0 || o0 >= p->O[0]) continue;
+                    for (int64_t i1 = 0; i1 < p->I[1]; ++i1) {
+                        const int64_t o1 = i1 * p->S[1] - p->PL[1] + t1 * p->DL[1];
+                        if (o1 < 0 || o1 >= p->O[1]) continue;
+                        const double* xr = xs + (i0 * p->I[1] + i1) * p->I[2];
+                        const double* dyr = dys + (o0 * p->O[1] + o1) * p->O[2];
+                        for (int64_t i2 = 0; i2 < p->I[2]; ++i2) {
+                            const int64_t o2 = i2 * p->S[2] - p->PL[2] + t2 * p->DL[2];
+                            if (o2 < 0 || o2 >= p->O[2]) continue;
+                            acc += xr[i2] * dyr[o2];
+                        }
+                    }
+                }
+            }
+            j->dw[(ic * Cog + oc_g) * Kn + (t0 * p->K[1] + t1) * p->K[2] + t2] = acc;
+        }
+    }
+}
+
+/* db[oc]: every output element of channel oc, batch by batch. */
+static void or_db_slice(const or_bjob* j, int64_t oc)
+{
+    const or_problem* p = j->p;
+    const int64_t On = p->O[0] * p->O[1] * p->O[2];
+    double acc = 0.0;
+    for (int64_t b = 0; b < p->B; ++b) {
+        const double* dys = j->dy + (b * p->C_out + oc) * On;
+        for (int64_t o = 0; o < On; ++o) acc += dys[o];
+    }
+    j->db[oc] = acc;
+}
+
+static void* or_bworker(void* arg)
+{
+    or_bjob* j = (or_bjob*)arg;
+    const or_problem* p = j->p;
+    const int64_t n_dx = j->dx ? p->B * p->C_in : 0;
+    const int64_t n_dw = j->dw ? p->C_in : 0;
+    const int64_t n_db = j->db ? p->C_out : 0;
+    for (;;) {
+        pthread_mutex_lock(&j->lock);
+        int64_t s = j->next_task++;
+        pthread_mutex_unlock(&j->lock);
+        if (s < n_dx) { or_dx_slice(j, s / p->C_in, s % p->C_in); continue; }
+        s -= n_dx;
+        if (s < n_dw) { or_dw_slice(j, s); continue; }
+        s -= n_dw;
+        if (s < n_db) { or_db_slice(j, s); continue; }
+        break;
+    }
+    return NULL;
+}
+
+/*
+ * Gradients of y = ConvTranspose(x, w, bias) with respect to x, w and the
+ * bias for an upstream gradient dy, in fp64.  Layouts as in
+ * oracle_conv_transpose_f64; dy has y's shape.  dx, dw and db may each be
+ * NULL (not computed).  Returns OR_OK or a nonzero code for invalid arguments.
+ */
+int oracle_conv_transpose_backward_f64(const double* x, const double* w,
+                                       const double* dy, double* dx, double* dw,
+                                       double* db, int nd, int64_t B,
+                                       int64_t C_in, int64_t C_out, int64_t groups,
+                                       const int64_t* in_sp, const int64_t* k,
+                                       const int64_t* stride, const int64_t* pad_lo,
+                                       const int64_t* pad_hi, const int64_t* dilation,
+                                       const int64_t* out_pad, int nthreads)
+{
+    or_problem p;
+    int rc = or_setup(&p, nd, B, C_in, C_out, groups, in_sp, k, stride,
+                      pad_lo, pad_hi, dilation, out_pad);
+    if (rc != OR_OK) return rc;
+    or_bjob j;
+    j.p = &p; j.x = x; j.w = w; j.dy = dy; j.dx = dx; j.dw = dw; j.db = db;
+    j.next_task = 0;
+    pthread_mutex_init(&j.lock, NULL);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t tid[256];
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tid[started], NULL, or_bworker, &j) != 0) break;
+        ++started;
+    }
+    or_bworker(&j);
+    for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+    pthread_mutex_destroy(&j.lock);
     return OR_OK;
 }

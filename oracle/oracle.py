@@ -55,6 +55,10 @@ def _lib():
         lib.oracle_conv_transpose_f64.argtypes = (
             [_f64p] * 4 + [ctypes.c_int] + [ctypes.c_int64] * 4 + [_i64p] * 7
             + [ctypes.c_int])
+        lib.oracle_conv_transpose_backward_f64.restype = ctypes.c_int
+        lib.oracle_conv_transpose_backward_f64.argtypes = (
+            [_f64p] * 6 + [ctypes.c_int] + [ctypes.c_int64] * 4 + [_i64p] * 7
+            + [ctypes.c_int])
         lib.oracle_points_f64.restype = ctypes.c_int
         lib.oracle_points_f64.argtypes = (
             [_f64p] * 3 + [ctypes.c_int] + [ctypes.c_int64] * 4 + [_i64p] * 7
@@ -185,3 +189,36 @@ def points(x, w, bias, idx, stride=None, pad_lo=None, pad_hi=None,
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (code {rc})")
     return out
+
+
+def conv_transpose_backward(x, w, dy, stride=None, pad_lo=None, pad_hi=None,
+                            dilation=None, output_padding=None, groups=1,
+                            threads=None, need=("dx", "dw", "db")):
+    """(dx, dw, db) for y = ConvTranspose(x, w, bias) and upstream gradient dy,
+    in float64: the adjoint of the scatter-add (SKaiNET #1464, Summary,
+    convTranspose2dBackward: input, weight and bias gradients).  Entries not
+    in `need` are None.
+    """
+    xd, wd, dyd = to_f64(x), to_f64(w), to_f64(dy)
+    nd = xd.ndim - 2
+    if nd < 1 or nd > 3 or wd.ndim != nd + 2 or dyd.ndim != nd + 2:
+        raise ValueError("x, dy must be [B, C, *spatial] and w [C_in, C_out/groups, *k]")
+    B, C_in = xd.shape[0], xd.shape[1]
+    C_out = wd.shape[1] * groups
+    I = _arr64(xd.shape[2:], nd, "in_spatial")
+    K = _arr64(wd.shape[2:], nd, "k")
+    S, PL, PH, DL, OP = _norm(nd, stride, pad_lo, pad_hi, dilation, output_padding)
+    O = out_shape(I, K, S, PL, PH, DL, OP)
+    if dyd.shape != (B, C_out) + O:
+        raise ValueError(f"dy must have the output shape {(B, C_out) + O}")
+    dx = np.empty(xd.shape, dtype=np.float64) if "dx" in need else None
+    dw = np.empty(wd.shape, dtype=np.float64) if "dw" in need else None
+    db = np.empty((C_out,), dtype=np.float64) if "db" in need else None
+    if threads is None:
+        threads = os.cpu_count() or 1
+    rc = _lib().oracle_conv_transpose_backward_f64(
+        _fp(xd), _fp(wd), _fp(dyd), _fp(dx), _fp(dw), _fp(db), nd, B, C_in, C_out,
+        groups, _ip(I), _ip(K), _ip(S), _ip(PL), _ip(PH), _ip(DL), _ip(OP), int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return dx, dw, db

@@ -83,9 +83,15 @@ def test_unmutated_copy_agrees(tmp_path):
     assert not _disagrees(f)
 
 
+# the forward part of the file; the backward oracle after this marker has
+# its own mutants (test_oracle_backward_pins)
+MARK = " * Backward pass (gradients), in fp64"
+
+
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_mutant_is_caught(tmp_path, name, old, new):
     text = open(SRC).read()
-    assert text.count(old) == 1, f"mutation site for '{name}' not unique"
-    f = _build(tmp_path, text.replace(old, new), "mut")
+    head, tail = text.split(MARK, 1)
+    assert head.count(old) == 1, f"mutation site for '{name}' not unique"
+    f = _build(tmp_path, head.replace(old, new) + MARK + tail, "mut")
     assert _disagrees(f), f"planted mistake '{name}' was not caught"
