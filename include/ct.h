@@ -247,6 +247,48 @@ int ct_conv_transpose_nd_host(const void* x, const void* w, const void* bias,
                               int groups, int dtype, void* stream);
 
 /*
+ * Gradients of y = ConvTranspose(x, w, bias): the backward pass of the
+ * SKaiNET pull request "feat(ops): implement convTranspose2d -- CPU kernel,
+ * backward and StableHLO lowering" (#1464, Summary: convTranspose2dBackward,
+ * the adjoint giving input, weight and bias gradients), for the same
+ * problems as ct_conv_transpose_nd.  For an upstream gradient dy (y's shape
+ * [B, C_out, out spatial...]):
+ *   dx[b, ic, i]    = sum_{oc in ic's group, t} w[ic, oc_g, t] * dy[b, oc, o(i, t)]
+ *   dw[ic, oc_g, t] = sum_{b, i}               x[b, ic, i]    * dy[b, oc, o(i, t)]
+ *   db[oc]          = sum_{b, o}               dy[b, oc, o]
+ * with o_a(i, t) = i_a*stride_a - pad_lo_a + t_a*dilation_a, terms whose o
+ * falls outside the output dropped.  All pointers are device pointers owned
+ * by the caller, dense, in the layouts of the forward call and one dtype;
+ * dx ([B, C_in, in spatial...]), dw ([C_in, C_out/groups, k...]) and db
+ * ([C_out]) may each be NULL (not computed); x is needed for dw, w for dx.
+ * Each result is written, not accumulated into.  fp32 accumulation, one
+ * rounding to the dtype, fixed summation order (bit-reproducible).
+ * workspace: device buffer of ct_conv_transpose_backward_workspace_bytes
+ * (256-byte aligned), or NULL to have the call allocate it stream-ordered.
+ * Asynchronous on `stream`.  Errors as the forward call; CT_ERR_TOO_LARGE
+ * when the kernel has more taps than the staged weight slab holds.
+ */
+int ct_conv_transpose_backward_nd(const void* x, const void* w, const void* dy,
+                                  void* dx, void* dw, void* db, void* workspace,
+                                  size_t workspace_bytes, int nd, int64_t B,
+                                  int64_t C_in, int64_t C_out,
+                                  const int64_t* in_spatial, const int64_t* k,
+                                  const int* stride, const int* pad_lo,
+                                  const int* pad_hi, const int* dilation,
+                                  const int* output_padding, int groups,
+                                  int dtype, void* stream);
+
+/* Workspace bytes of ct_conv_transpose_backward_nd (dw's per-slice partials). */
+int ct_conv_transpose_backward_workspace_bytes(int nd, int64_t B, int64_t C_in,
+                                               int64_t C_out,
+                                               const int64_t* in_spatial,
+                                               const int64_t* k, const int* stride,
+                                               const int* pad_lo, const int* pad_hi,
+                                               const int* dilation,
+                                               const int* output_padding,
+                                               int groups, int dtype, size_t* bytes);
+
+/*
  * Returns the memory the host-buffer entry point keeps in its pool on the
  * current device to the device (the pool itself stays, empty).  The memory
  * is otherwise kept until process exit.  Host only; CT_ERR_CUDA on failure.

@@ -1,0 +1,157 @@
+"""GPU parity of the backward pass (dx, dw, db) against the fp64 oracle.
+
+The oracle's gradients are the adjoint of its scatter-add, pinned in
+test_oracle_backward_pins.  Bars: max|g - g_oracle| <= 1e-5 * max|g_oracle|
+for fp32 and 1e-2 * max|g_oracle| for bf16/fp16 (each gradient on its own),
+computed on the values the device sees (16-bit inputs widened exactly).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import transposed_convolution_convtranspose1_gb300 as ct
+from transposed_convolution_convtranspose1_gb300 import synth
+from _parity import TOL
+
+pytestmark = pytest.mark.gpu
+
+P = synth.problem
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from transposed_convolution_convtranspose1_gb300 import _build
+    _build.build_library()
+    ct.lib()
+    yield
+
+
+def _dy_for(p, seed):
+    O = ct.ct_conv_transpose_out_shape(p.spatial, p.k, p.stride, p.pad_lo, p.pad_hi,
+                                       p.dilation, p.output_padding)
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn((p.B, p.C_out) + tuple(O), generator=g).to(p.torch_dtype)
+
+
+def _gpu_grads(p, x, w, dy, need=("dx", "dw", "db")):
+    xd, wd, dyd = x.cuda(), w.cuda(), dy.cuda()
+    dx = torch.full_like(xd, float("nan")) if "dx" in need else None
+    dw = torch.full_like(wd, float("nan")) if "dw" in need else None
+    db = torch.full((p.C_out,), float("nan"), dtype=dyd.dtype, device="cuda") if "db" in need else None
+    ct.ct_conv_transpose_backward_nd(xd, wd, dyd, dx, dw, db, None, p.stride, p.pad_lo, p.pad_hi,
+                                     p.dilation, p.output_padding, p.groups)
+    torch.cuda.synchronize()
+    return dx, dw, db
+
+
+def _check(p, got, ref, what):
+    if ref.size == 0:
+        assert got.numel() == 0
+        return
+    g = got.to(torch.float64).cpu().numpy()
+    assert g.shape == ref.shape, (what, g.shape, ref.shape)
+    scale = float(np.max(np.abs(ref)))
+    err = float(np.max(np.abs(g - ref)))
+    assert np.isfinite(g).all(), f"{p.name} {what}: non-finite values"
+    assert err <= TOL[p.dtype] * scale + 1e-30, f"{p.name} {what}: max|err| {err:.3e} > {TOL[p.dtype]:.0e} * {scale:.3e}"
+
+
+def _check_all(p, seed=0):
+    x, w, _ = synth.make_inputs(p)
+    dy = _dy_for(p, 1000 + seed)
+    rdx, rdw, rdb = oracle.conv_transpose_backward(x, w, dy, **p.attrs())
+    dx, dw, db = _gpu_grads(p, x, w, dy)
+    _check(p, dx, rdx, "dx")
+    _check(p, dw, rdw, "dw")
+    _check(p, db, rdb, "db")
+
+
+def _grid():
+    r = np.random.default_rng(1234)
+    out = []
+    for n in range(30):
+        nd = int(r.integers(1, 4))
+        G = int(r.choice([1, 1, 2, 4]))
+        Cig, Cog = int(r.integers(1, 20)), int(r.integers(1, 20))
+        spatial, k, s, pl, ph, d, op = [], [], [], [], [], [], []
+        for _ in range(nd):
+            spatial.append(int(r.integers(1, 12 if nd < 3 else 6)))
+            k.append(int(r.integers(1, 5)))
+            s.append(int(r.integers(1, 4)))
+            d.append(int(r.integers(1, 3)))
+            op.append(int(r.integers(0, max(s[-1], d[-1]))))
+            while True:
+                a, b = int(r.integers(0, 3)), int(r.integers(0, 3))
+                if (spatial[-1] - 1) * s[-1] - a - b + d[-1] * (k[-1] - 1) + op[-1] + 1 >= 1:
+                    break
+            pl.append(a)
+            ph.append(b)
+        dtype = str(r.choice(["f32", "f32", "bf16", "f16"]))
+        out.append(P(f"bwd{n}_{nd}d_{dtype}_g{G}", int(r.integers(1, 4)), G * Cig, G * Cog,
+                     tuple(spatial), tuple(k), stride=tuple(s), pad_lo=tuple(pl), pad_hi=tuple(ph),
+                     dilation=tuple(d), output_padding=tuple(op), groups=G, dtype=dtype,
+                     seed=2000 + n))
+    return out
+
+
+@pytest.mark.parametrize("p", _grid(), ids=lambda p: p.name)
+def test_backward_grid_matches_oracle(p):
+    _check_all(p)
+
+
+@pytest.mark.parametrize("i", [0, 1, 3])
+def test_backward_workload_matches_oracle(i):
+    _check_all(synth.workload(i))
+
+
+def test_backward_bf16_workload_matches_oracle():
+    p = synth.workload(2).replace(B=2)  # the 2-D bf16 workload, batch 2
+    _check_all(p)
+
+
+def test_backward_is_bit_reproducible_and_partial_requests_agree():
+    p = synth.workload(3).replace(B=2)
+    x, w, _ = synth.make_inputs(p)
+    dy = _dy_for(p, 5)
+    a = _gpu_grads(p, x, w, dy)
+    b = _gpu_grads(p, x, w, dy)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+    only_dw = _gpu_grads(p, x, w, dy, need=("dw",))
+    assert only_dw[0] is None and only_dw[2] is None
+    assert torch.equal(only_dw[1], a[1])
+    only_dx = _gpu_grads(p, x, w, dy, need=("dx",))
+    assert torch.equal(only_dx[0], a[0])
+
+
+def test_backward_empty_batch_gives_zero_weight_and_bias_gradients():
+    p = P("bwd_empty", 0, 4, 6, (5,), 3, stride=2)
+    x = torch.zeros((0, 4, 5))
+    w = synth.make_inputs(p.replace(B=1))[1]
+    dy = torch.zeros((0, 6, 11))
+    dx, dw, db = _gpu_grads(p, x, w, dy)
+    assert dx.numel() == 0
+    assert torch.equal(dw.cpu(), torch.zeros_like(w))
+    assert torch.equal(db.cpu(), torch.zeros(6))
+
+
+def test_autograd_function_matches_torch():
+    """ConvTransposeFunction's fp32 gradients against torch's own
+    conv_transpose2d autograd run in float64 on the same values, within the
+    fp32 bound relative to the largest gradient."""
+    p = P("autograd", 2, 16, 24, (9, 7), 3, stride=2, pad=1, output_padding=1, seed=77)
+    x, w, b = synth.make_inputs(p)
+    dy = _dy_for(p, 9)
+    x0, w0, b0 = (t.cuda().requires_grad_(True) for t in (x, w, b))
+    x1, w1, b1 = (t.cuda().double().requires_grad_(True) for t in (x, w, b))
+    y0 = ct.conv_transpose_autograd(x0, w0, b0, stride=2, padding=1, output_padding=1)
+    y1 = torch.nn.functional.conv_transpose2d(x1, w1, b1, stride=2, padding=1, output_padding=1)
+    assert float((y0.double() - y1).detach().abs().max()) <= 1e-5 * float(y1.detach().abs().max())
+    y0.backward(dy.cuda())
+    y1.backward(dy.cuda().double())
+    for a, c in ((x0.grad, x1.grad), (w0.grad, w1.grad), (b0.grad, b1.grad)):
+        scale = float(c.abs().max())
+        assert float((a.double() - c).abs().max()) <= 1e-5 * scale

@@ -13,4 +13,5 @@ from .ct import (  # noqa: F401
     ct_conv_transpose_nd_noalloc, CT_NOALLOC_SCRATCH_BYTES,
     ct_conv_transpose_out_shape, ct_conv_transpose_route, ct_conv_transpose_workspace_bytes,
     ct_device_status, ct_host_buffers_release, ct_last_error, ct_status_string, ct_version,
-    dtype_code, lib)
+    dtype_code, lib, ct_conv_transpose_backward_nd, ct_conv_transpose_backward_workspace_bytes,
+    conv_transpose_backward, ConvTransposeFunction, conv_transpose_autograd)

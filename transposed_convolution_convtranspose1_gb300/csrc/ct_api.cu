@@ -519,6 +519,69 @@ int ct_conv_transpose_nd_host(const void* x, const void* w, const void* bias, vo
     return rc;
 }
 
+int ct_conv_transpose_backward_workspace_bytes(int nd, int64_t B, int64_t C_in, int64_t C_out,
+                                               const int64_t* in_spatial, const int64_t* k,
+                                               const int* stride, const int* pad_lo,
+                                               const int* pad_hi, const int* dilation,
+                                               const int* output_padding, int groups, int dtype,
+                                               size_t* bytes) {
+    if (!bytes) return fail(CT_ERR_NULL, "bytes is NULL");
+    Problem p;
+    int rc = validate(&p, nd, B, C_in, C_out, in_spatial, k, stride, pad_lo, pad_hi, dilation,
+                      output_padding, groups, dtype);
+    if (rc != CT_OK) return rc;
+    if (!backward_supported(p))
+        return fail(CT_ERR_TOO_LARGE, "backward: %lld taps per input channel block exceed the staged slab",
+                    (long long)p.taps());
+    *bytes = backward_workspace_bytes(p);
+    return CT_OK;
+}
+
+int ct_conv_transpose_backward_nd(const void* x, const void* w, const void* dy, void* dx, void* dw,
+                                  void* db, void* workspace, size_t workspace_bytes, int nd,
+                                  int64_t B, int64_t C_in, int64_t C_out,
+                                  const int64_t* in_spatial, const int64_t* k, const int* stride,
+                                  const int* pad_lo, const int* pad_hi, const int* dilation,
+                                  const int* output_padding, int groups, int dtype, void* stream) {
+    Problem p;
+    int rc = validate(&p, nd, B, C_in, C_out, in_spatial, k, stride, pad_lo, pad_hi, dilation,
+                      output_padding, groups, dtype);
+    if (rc != CT_OK) return rc;
+    const bool need_dy = dx || dw || db;
+    if ((need_dy && p.y_elems() > 0 && !dy) || (dx && p.x_elems() > 0 && !w) ||
+        (dw && p.w_elems() > 0 && p.x_elems() > 0 && !x))
+        return fail(CT_ERR_NULL, "backward: dy (and w for dx, x for dw) must not be NULL");
+    const size_t eb = p.elem_bytes();
+    for (const void* q : {x, w, dy, (const void*)dx, (const void*)dw, (const void*)db})
+        if (q && !aligned(q, eb)) return fail(CT_ERR_ALIGN, "pointers must be aligned to the element size (%zu bytes)", eb);
+    if (!backward_supported(p))
+        return fail(CT_ERR_TOO_LARGE, "backward: %lld taps per input channel block exceed the staged slab",
+                    (long long)p.taps());
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t need = dw ? backward_workspace_bytes(p) : 0;
+    void* ws = workspace;
+    bool owned = false;
+    if (need > 0) {
+        if (ws) {
+            if (workspace_bytes < need)
+                return fail(CT_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
+                            workspace_bytes, need);
+            if (!aligned(ws, 256)) return fail(CT_ERR_ALIGN, "workspace must be 256-byte aligned");
+        } else {
+            cudaError_t e = cudaMallocAsync(&ws, need, s);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(backward workspace)");
+            owned = true;
+        }
+    }
+    cudaError_t e = launch_backward(p, x, w, dy, dx, dw, db, ws, s, nullptr);
+    if (owned) {
+        cudaError_t e2 = cudaFreeAsync(ws, s);
+        if (e == cudaSuccess) e = e2;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "backward kernel launch");
+    return CT_OK;
+}
+
 int ct_host_buffers_release(void) {
     HostRes* R = nullptr;
     cudaError_t e = host_resources(&R);

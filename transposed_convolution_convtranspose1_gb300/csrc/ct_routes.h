@@ -34,6 +34,14 @@ size_t tc32_workspace_bytes(const Problem& p);
 cudaError_t launch_tc32(const Problem& p, const void* x, const void* w, const void* bias, void* y,
                         void* workspace, cudaStream_t stream, Profile* prof);
 
+// Gradients of the transposed convolution on CUDA cores (ct_backward.cu):
+// dx, dw and db, each skipped when its pointer is null.  The workspace holds
+// dw's per-slice fp32 partials.  `launches` (optional) counts the kernels.
+bool backward_supported(const Problem& p);
+size_t backward_workspace_bytes(const Problem& p);
+cudaError_t launch_backward(const Problem& p, const void* x, const void* w, const void* dy, void* dx,
+                            void* dw, void* db, void* workspace, cudaStream_t stream, int* launches);
+
 // Device error words of the tcgen05 routes: codes recorded by bounded waits
 // that timed out (0 = none); `clear` resets a non-zero word.
 cudaError_t tc_error_word(unsigned int* v, bool clear);

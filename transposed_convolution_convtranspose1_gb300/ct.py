@@ -48,7 +48,8 @@ EXPORTS = ("ct_version", "ct_last_error", "ct_status_string",
            "ct_conv_transpose_route", "ct_conv_transpose_route_workspace_bytes",
            "ct_conv_transpose_nd", "ct_conv_transpose_nd_route",
            "ct_conv_transpose_nd_host", "ct_conv_transpose_nd_profiled",
-           "ct_conv_transpose_nd_noalloc", "ct_device_status", "ct_host_buffers_release")
+           "ct_conv_transpose_nd_noalloc", "ct_device_status", "ct_host_buffers_release",
+           "ct_conv_transpose_backward_nd", "ct_conv_transpose_backward_workspace_bytes")
 
 # Size of the static scratch behind ct_conv_transpose_nd_noalloc (CT_NOALLOC_SCRATCH_BYTES).
 CT_NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -108,6 +109,11 @@ def _declare(h):
     h.ct_device_status.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_uint)]
     h.ct_host_buffers_release.restype = ctypes.c_int
     h.ct_host_buffers_release.argtypes = []
+    h.ct_conv_transpose_backward_nd.restype = ctypes.c_int
+    h.ct_conv_transpose_backward_nd.argtypes = ([_vp] * 7 + [ctypes.c_size_t] + _SHAPE_ARGS + [_vp])
+    h.ct_conv_transpose_backward_workspace_bytes.restype = ctypes.c_int
+    h.ct_conv_transpose_backward_workspace_bytes.argtypes = _SHAPE_ARGS + [
+        ctypes.POINTER(ctypes.c_size_t)]
 
 
 def lib():
@@ -353,3 +359,78 @@ def conv_transpose(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor
     y = torch.empty((B, C_out) + O, dtype=x.dtype, device=x.device)
     ct_conv_transpose_nd(x, w, bias, y, workspace, s, pl, ph, d, op, groups, route)
     return y
+
+
+def ct_conv_transpose_backward_workspace_bytes(B, C_in, C_out, in_spatial, k, stride=None,
+                                               pad_lo=None, pad_hi=None, dilation=None,
+                                               output_padding=None, groups=1,
+                                               dtype=CT_F32) -> int:
+    ax = _Axes(len(in_spatial), in_spatial, k, stride, pad_lo, pad_hi, dilation, output_padding)
+    n = ctypes.c_size_t(0)
+    _check(lib().ct_conv_transpose_backward_workspace_bytes(
+        *_shape_args(B, C_in, C_out, ax, groups, dtype), ctypes.byref(n)))
+    return int(n.value)
+
+
+def ct_conv_transpose_backward_nd(x: torch.Tensor, w: torch.Tensor, dy: torch.Tensor,
+                                  dx: Optional[torch.Tensor] = None,
+                                  dw: Optional[torch.Tensor] = None,
+                                  db: Optional[torch.Tensor] = None,
+                                  workspace: Optional[torch.Tensor] = None, stride=None,
+                                  pad_lo=None, pad_hi=None, dilation=None, output_padding=None,
+                                  groups: int = 1, stream=None) -> None:
+    """Run the backward entry point on torch CUDA tensors; dx, dw and db (any
+    may be None) are overwritten."""
+    nd, B, C_in, C_out, I, K = _problem_from_tensors(x, w, groups)
+    ax = _Axes(nd, I, K, stride, pad_lo, pad_hi, dilation, output_padding)
+    nws = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    s = _stream_handle(stream, dy.device)
+    _check(lib().ct_conv_transpose_backward_nd(
+        _ptr(x), _ptr(w), _ptr(dy), _ptr(dx), _ptr(dw), _ptr(db), _ptr(workspace), nws,
+        *_shape_args(B, C_in, C_out, ax, groups, dtype_code(dy.dtype)), s))
+
+
+def conv_transpose_backward(x: torch.Tensor, w: torch.Tensor, dy: torch.Tensor, stride=1,
+                            padding=0, pad_lo=None, pad_hi=None, dilation=1, output_padding=0,
+                            groups: int = 1, need=("dx", "dw", "db")):
+    """Allocate and return (dx, dw, db) for upstream gradient dy; entries not
+    in `need` are None."""
+    nd, B, C_in, C_out, I, K = _problem_from_tensors(x, w, groups)
+    s, pl, ph, d, op = _attrs(nd, stride, padding, pad_lo, pad_hi, dilation, output_padding)
+    dx = torch.empty_like(x) if "dx" in need else None
+    dw = torch.empty_like(w) if "dw" in need else None
+    db = torch.empty((C_out,), dtype=dy.dtype, device=dy.device) if "db" in need else None
+    ct_conv_transpose_backward_nd(x, w, dy, dx, dw, db, None, s, pl, ph, d, op, groups)
+    return dx, dw, db
+
+
+class ConvTransposeFunction(torch.autograd.Function):
+    """torch.autograd binding: forward and backward both run in libct.so."""
+
+    @staticmethod
+    def forward(ctx, x, w, bias, stride, padding, pad_lo, pad_hi, dilation, output_padding,
+                groups):
+        ctx.save_for_backward(x, w)
+        ctx.attrs = (stride, padding, pad_lo, pad_hi, dilation, output_padding, groups)
+        ctx.has_bias = bias is not None
+        return conv_transpose(x, w, bias, stride, padding, pad_lo, pad_hi, dilation,
+                              output_padding, groups)
+
+    @staticmethod
+    def backward(ctx, dy):
+        x, w = ctx.saved_tensors
+        stride, padding, pad_lo, pad_hi, dilation, output_padding, groups = ctx.attrs
+        need = tuple(n for n, flag in (("dx", ctx.needs_input_grad[0]),
+                                       ("dw", ctx.needs_input_grad[1]),
+                                       ("db", ctx.needs_input_grad[2] and ctx.has_bias)) if flag)
+        dx, dw, db = conv_transpose_backward(x, w, dy.contiguous(), stride, padding, pad_lo,
+                                             pad_hi, dilation, output_padding, groups, need)
+        return (dx, dw, db, None, None, None, None, None, None, None)
+
+
+def conv_transpose_autograd(x, w, bias=None, stride=1, padding=0, pad_lo=None, pad_hi=None,
+                            dilation=1, output_padding=0, groups=1):
+    """conv_transpose that records itself for torch.autograd."""
+    return ConvTransposeFunction.apply(x, w, bias, stride, padding, pad_lo, pad_hi, dilation,
+                                       output_padding, groups)
+
