@@ -12,6 +12,8 @@ metric  : ConvTranspose TFLOP/s (valid multiply-adds x 2 / time); the HBM
 e2e     : the same metric through ct_conv_transpose_nd_host with pinned host
           buffers (host-to-device copies of x, w, bias and the device-to-host
           copy of y inside the timed region).
+backward : each gradient (dx, dw, db) of every workload timed on its own
+          through ct_conv_transpose_backward_nd (skip with --no-backward).
 --impl reference : the fp64 CPU oracle timed on the host cores on a bounded
           sample of the same workload (the only other place this script runs
           the oracle is the cpu_baseline leg).
@@ -442,6 +444,8 @@ def run_ours(args):
 
     if not args.no_per_config and world == 1:
         line["per_config"] = per_config(args, dev, peaks, flush, skip=p.name)
+    if not args.no_backward and world == 1:
+        line["backward"] = backward_per_config(dev, flush, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p, args.cpu_seconds)
     if rank == 0:
@@ -470,6 +474,60 @@ def per_config(args, dev, peaks, flush, skip):
             "roofline": roofline(route_name, p, main, peaks, timed_alone=True),
             "steps": K, "stat": "median"}
         del r
+        torch.cuda.empty_cache()
+    return out
+
+
+def backward_per_config(dev, flush, peaks):
+    """Each gradient of every workload timed on its own (events around a call
+    that requests only it, L2 flushed before each): dx and dw against the fp32
+    FMA peak (CUDA-core kernels; work = the forward's 2 x valid MACs each), db
+    against HBM bandwidth (dy read once)."""
+    import transposed_convolution_convtranspose1_gb300 as ct
+    out = {}
+    for p in synth.WORKLOADS:
+        x, w, _ = synth.make_inputs(p)
+        x, w = x.to(dev), w.to(dev)
+        O = out_shape(p)
+        g = torch.Generator().manual_seed(4242)
+        dy = torch.randn((p.B, p.C_out) + O, generator=g).to(p.torch_dtype).to(dev)
+        dx, dw = torch.empty_like(x), torch.empty_like(w)
+        db = torch.empty((p.C_out,), dtype=dy.dtype, device=dev)
+        nws = ct.ct_conv_transpose_backward_workspace_bytes(
+            p.B, p.C_in, p.C_out, p.spatial, p.k, p.stride, p.pad_lo, p.pad_hi, p.dilation,
+            p.output_padding, p.groups, ct.dtype_code(p.torch_dtype))
+        ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
+        flops = 2.0 * valid_macs(p)
+        res = {}
+        for name, args in (("dx", (dx, None, None)), ("dw", (None, dw, None)),
+                           ("db", (None, None, db))):
+            def call():
+                ct.ct_conv_transpose_backward_nd(x, w, dy, *args, ws, p.stride, p.pad_lo,
+                                                 p.pad_hi, p.dilation, p.output_padding, p.groups)
+            for _ in range(3):
+                call()
+            K = 10
+            e0, e1 = _events(K), _events(K)
+            torch.cuda.synchronize()
+            for i in range(K):
+                if flush is not None:
+                    flush.add_(1)
+                e0[i].record()
+                call()
+                e1[i].record()
+            torch.cuda.synchronize()
+            ms = statistics.median([a.elapsed_time(b) for a, b in zip(e0, e1)])
+            if name == "db":
+                nbytes = dy.numel() * dy.element_size() + p.C_out * dy.element_size()
+                ach = nbytes / (ms * 1e-3) / 1e9
+                res[name] = {"ms": round(ms, 5), "achieved": round(ach, 2), "unit": "GB/s",
+                             "bound": "hbm", "frac": round(ach / peaks["hbm_gbs"], 4)}
+            else:
+                ach = flops / (ms * 1e-3) / 1e12
+                res[name] = {"ms": round(ms, 5), "achieved": round(ach, 3), "unit": "TFLOP/s",
+                             "bound": "alu", "frac": round(ach / FP32_ALU_PEAK_TFLOPS, 4)}
+        out[p.name] = res
+        del x, w, dy, dx, dw, db, ws
         torch.cuda.empty_cache()
     return out
 
@@ -552,6 +610,8 @@ def main():
     ap.add_argument("--config", default="1", help="workload index 0-4 or name (default 1)")
     ap.add_argument("--no-flush", action="store_true")
     ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the per-workload gradient timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
