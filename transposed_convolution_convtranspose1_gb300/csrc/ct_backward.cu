@@ -16,20 +16,21 @@
 // tensor dtype, no atomics: every result is summed in a fixed order, so runs
 // are bit-reproducible):
 //   bwd_db_kernel   one block per output channel; each thread sums a strided
-//                   share of the channel with compensated (Kahan) fp32 adds,
-//                   then a fixed shared-memory tree.
+//                   share of the channel in four compensated (Kahan) fp32
+//                   sums, then a fixed shared-memory tree.
 //   bwd_dx_kernel   one thread per input position and ICB input channels of
 //                   a group; the group's weights for a chunk of output
 //                   channels are staged in shared memory ([oc][tap][ICB]) and
 //                   read as broadcasts; per tap the thread finds the output
 //                   position its input fed (or none) once, then walks the
 //                   chunk's output channels.
-//   bwd_dw_kernel   per (group, tile of 32 input channels, tile of 32
+//   bwd_dw_kernel   per (group, tile of 64 input channels, tile of 64
 //                   (output channel, tap) pairs, K slice): the slice's
-//                   positions are staged 64 at a time, one column per thread
-//                   (x rows and the dy values each (oc, tap) pair reads, zero
-//                   where the tap falls outside the output); 64 threads,
-//                   each a 4 x 4 register tile.  Slices write fp32
+//                   positions are staged 32 at a time, a thread loading 8
+//                   rows of one column (x rows and the dy values each (oc,
+//                   tap) pair reads, zero where the tap falls outside the
+//                   output) before storing any; 256 threads, each a 4 x 4
+//                   register tile.  Slices write fp32
 //                   partials; bwd_dw_reduce adds them in slice order and
 //                   rounds once.
 #include <algorithm>
@@ -63,24 +64,35 @@ struct BwdArgs {
 // db
 // ---------------------------------------------------------------------------
 
-constexpr int kDbThreads = 256;
+constexpr int kDbThreads = 512;
 
 template <typename T>
 __global__ void __launch_bounds__(kDbThreads) bwd_db_kernel(const __grid_constant__ BwdArgs a) {
     __shared__ float red[kDbThreads];
     const int64_t oc = blockIdx.x;
     const T* __restrict__ dy = static_cast<const T*>(a.dy);
-    float sum = 0.f, comp = 0.f;  // Kahan: comp holds the lost low-order part
+    // four independent compensated (Kahan) sums per thread, so that four
+    // loads are in flight; comp holds each sum's lost low-order part
+    float sum[4] = {0.f, 0.f, 0.f, 0.f}, comp[4] = {0.f, 0.f, 0.f, 0.f};
     for (int64_t b = 0; b < a.B; ++b) {
         const T* p = dy + (b * a.C_out + oc) * a.On;
-        for (int64_t o = threadIdx.x; o < a.On; o += kDbThreads) {
-            const float v = to_f32(p[o]) - comp;
-            const float t = sum + v;
-            comp = (t - sum) - v;
-            sum = t;
+        for (int64_t o = threadIdx.x; o < a.On; o += 4 * kDbThreads) {
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t ou = o + (int64_t)u * kDbThreads;
+                v[u] = ou < a.On ? to_f32(p[ou]) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float y = v[u] - comp[u];
+                const float t = sum[u] + y;
+                comp[u] = (t - sum[u]) - y;
+                sum[u] = t;
+            }
         }
     }
-    red[threadIdx.x] = sum;
+    red[threadIdx.x] = (sum[0] + sum[1]) + (sum[2] + sum[3]);
     __syncthreads();
     for (int h = kDbThreads / 2; h > 0; h >>= 1) {
         if ((int)threadIdx.x < h) red[threadIdx.x] += red[threadIdx.x + h];
@@ -169,10 +181,11 @@ __global__ void __launch_bounds__(kDxThreads) bwd_dx_kernel(const __grid_constan
 // dw
 // ---------------------------------------------------------------------------
 
-constexpr int kDwTM = 32;     // input channels per tile
-constexpr int kDwTN = 32;     // (output channel, tap) pairs per tile
-constexpr int kDwTK = 64;     // positions staged per step
-constexpr int kDwThreads = 64;
+constexpr int kDwTM = 64;     // input channels per tile
+constexpr int kDwTN = 64;     // (output channel, tap) pairs per tile
+constexpr int kDwTK = 32;     // positions staged per step
+constexpr int kDwThreads = 256;
+constexpr int kDwRows = 8;    // staged rows per thread (of x and of dy)
 
 template <typename T>
 __global__ void __launch_bounds__(kDwThreads) bwd_dw_kernel(const __grid_constant__ BwdArgs a,
@@ -192,8 +205,21 @@ __global__ void __launch_bounds__(kDwThreads) bwd_dw_kernel(const __grid_constan
     const int64_t k_begin = (int64_t)ks * a.ks_len;
     const int64_t k_end = min((int64_t)(ks + 1) * a.ks_len, a.B * a.In);
 
-    // this thread's 4 x 4 outputs: rows tm * 4 .. +3, columns tn * 4 .. +3
-    const int tm = threadIdx.x / 8, tn = threadIdx.x % 8;
+    // compute: this thread's 4 x 4 outputs, rows tm * 4 .., columns tn * 4 ..
+    const int tm = threadIdx.x / 16, tn = threadIdx.x % 16;
+    // staging: column kk of the step, rows r0 .. r0 + kDwRows - 1
+    const int kk = threadIdx.x % kDwTK, r0 = (threadIdx.x / kDwTK) * kDwRows;
+    // the (oc_g, tap) pairs of this thread's staged dy rows
+    int n_oc[kDwRows], n_t[kDwRows][3];
+#pragma unroll
+    for (int r = 0; r < kDwRows; ++r) {
+        const int n = min(n0 + r0 + r, NN - 1);
+        const int t = n % a.Kn;
+        n_oc[r] = n / a.Kn;
+        n_t[r][2] = t % a.K[2];
+        n_t[r][1] = (t / a.K[2]) % a.K[1];
+        n_t[r][0] = t / (a.K[2] * a.K[1]);
+    }
     float acc[4][4];
 #pragma unroll
     for (int r = 0; r < 4; ++r)
@@ -201,54 +227,48 @@ __global__ void __launch_bounds__(kDwThreads) bwd_dw_kernel(const __grid_constan
         for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
 
     for (int64_t k0 = k_begin; k0 < k_end; k0 += kDwTK) {
-        __syncthreads();
-        // staging: thread kk owns column kk (one batch x position k) and walks
-        // the rows: x rows m (input channels), dy rows n = (oc_g, tap) at the
-        // output that position's tap wrote (zero where it falls outside)
-        {
-            const int kk = threadIdx.x;
-            const int64_t k = k0 + kk;
-            const bool kok = k < k_end;
-            int64_t b = 0, i = 0;
-            int i0 = 0, i1 = 0, i2 = 0;
-            if (kok) {
-                b = k / a.In;
-                i = k - b * a.In;
-                i2 = (int)(i % a.I[2]);
-                i1 = (int)((i / a.I[2]) % a.I[1]);
-                i0 = (int)(i / ((int64_t)a.I[2] * a.I[1]));
+        // load this thread's staged values (all loads before any store)
+        const int64_t k = k0 + kk;
+        const bool kok = k < k_end;
+        int64_t b = 0, i = 0;
+        int i0 = 0, i1 = 0, i2 = 0;
+        if (kok) {
+            b = k / a.In;
+            i = k - b * a.In;
+            i2 = (int)(i % a.I[2]);
+            i1 = (int)((i / a.I[2]) % a.I[1]);
+            i0 = (int)(i / ((int64_t)a.I[2] * a.I[1]));
+        }
+        float xv[kDwRows], dv[kDwRows];
+        const T* xp = x + (b * a.C_in + (int64_t)g * a.Cig + m0 + r0) * a.In + i;
+        const T* dyb = dy + (b * a.C_out + (int64_t)g * a.Cog) * a.On;
+#pragma unroll
+        for (int r = 0; r < kDwRows; ++r) {
+            xv[r] = (kok && m0 + r0 + r < a.Cig) ? to_f32(xp[(int64_t)r * a.In]) : 0.f;
+            float v = 0.f;
+            if (kok && n0 + r0 + r < NN) {
+                const int o0 = i0 * a.S[0] - a.PL[0] + n_t[r][0] * a.DL[0];
+                const int o1 = i1 * a.S[1] - a.PL[1] + n_t[r][1] * a.DL[1];
+                const int o2 = i2 * a.S[2] - a.PL[2] + n_t[r][2] * a.DL[2];
+                if (o0 >= 0 && o0 < a.O[0] && o1 >= 0 && o1 < a.O[1] && o2 >= 0 && o2 < a.O[2])
+                    v = to_f32(dyb[(int64_t)n_oc[r] * a.On + ((int64_t)o0 * a.O[1] + o1) * a.O[2] + o2]);
             }
-            const T* xp = x + (b * a.C_in + (int64_t)g * a.Cig + m0) * a.In + i;
-#pragma unroll 4
-            for (int m = 0; m < kDwTM; ++m)
-                xs[m][kk] = (kok && m0 + m < a.Cig) ? to_f32(xp[(int64_t)m * a.In]) : 0.f;
-            const T* dyb = dy + (b * a.C_out + (int64_t)g * a.Cog) * a.On;
-            int oc = n0 / a.Kn, t = n0 % a.Kn;
-            for (int nn = 0; nn < kDwTN; ++nn) {
-                float v = 0.f;
-                if (kok && n0 + nn < NN) {
-                    const int t2 = t % a.K[2], t1 = (t / a.K[2]) % a.K[1], t0 = t / (a.K[2] * a.K[1]);
-                    const int o0 = i0 * a.S[0] - a.PL[0] + t0 * a.DL[0];
-                    const int o1 = i1 * a.S[1] - a.PL[1] + t1 * a.DL[1];
-                    const int o2 = i2 * a.S[2] - a.PL[2] + t2 * a.DL[2];
-                    if (o0 >= 0 && o0 < a.O[0] && o1 >= 0 && o1 < a.O[1] && o2 >= 0 && o2 < a.O[2])
-                        v = to_f32(dyb[(int64_t)oc * a.On + ((int64_t)o0 * a.O[1] + o1) * a.O[2] + o2]);
-                }
-                ds[nn][kk] = v;
-                if (++t == a.Kn) {
-                    t = 0;
-                    ++oc;
-                }
-            }
+            dv[r] = v;
+        }
+        __syncthreads();  // the previous step's tiles are no longer read
+#pragma unroll
+        for (int r = 0; r < kDwRows; ++r) {
+            xs[r0 + r][kk] = xv[r];
+            ds[r0 + r][kk] = dv[r];
         }
         __syncthreads();
-#pragma unroll 4
-        for (int kk = 0; kk < kDwTK; kk += 4) {
+#pragma unroll 2
+        for (int q = 0; q < kDwTK; q += 4) {
             float4 xa[4], da[4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) xa[r] = *reinterpret_cast<const float4*>(&xs[tm * 4 + r][kk]);
+            for (int r = 0; r < 4; ++r) xa[r] = *reinterpret_cast<const float4*>(&xs[tm * 4 + r][q]);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) da[c] = *reinterpret_cast<const float4*>(&ds[tn * 4 + c][kk]);
+            for (int c = 0; c < 4; ++c) da[c] = *reinterpret_cast<const float4*>(&ds[tn * 4 + c][q]);
 #pragma unroll
             for (int r = 0; r < 4; ++r)
 #pragma unroll
