@@ -446,6 +446,8 @@ def run_ours(args):
         line["per_config"] = per_config(args, dev, peaks, flush, skip=p.name)
     if not args.no_backward and world == 1:
         line["backward"] = backward_per_config(dev, flush, peaks)
+        if rank == 0 and not args.no_cpu_baseline:
+            line["backward"]["cpu_baseline"] = backward_cpu_baseline(p, min(args.cpu_seconds, 10.0))
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p, args.cpu_seconds)
     if rank == 0:
@@ -564,6 +566,28 @@ def cpu_baseline(p, target_s):
             "kind": "oracle", "seconds": round(sum(times), 3), "runs": len(times),
             "sample": f"batch elements 0..{nb - 1} of {p.B} of {p.name} (fp64 scatter-add, "
                       f"{threads} threads), {len(times)} runs"}
+
+
+def backward_cpu_baseline(p, target_s):
+    """The backward oracle (dx and dw, fp64) on the host cores on one batch
+    element of the workload, repeated until about target_s have elapsed."""
+    import oracle
+    x, w, _ = synth.make_inputs(p.replace(B=1))
+    O = out_shape(p)
+    g = torch.Generator().manual_seed(4242)
+    dy = torch.randn((1, p.C_out) + O, generator=g).to(p.torch_dtype)
+    threads = os.cpu_count() or 1
+    times = []
+    while not times or (sum(times) < target_s and len(times) < 10):
+        t0 = time.perf_counter()
+        oracle.conv_transpose_backward(x, w, dy, **p.attrs(), threads=threads, need=("dx", "dw"))
+        times.append(time.perf_counter() - t0)
+    dt = statistics.mean(times)
+    flops = 2.0 * 2.0 * valid_macs(p.replace(B=1))  # dx and dw, each the forward's work
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "seconds": round(sum(times), 3), "runs": len(times),
+            "sample": f"dx and dw of batch element 0 of {p.B} of {p.name} (fp64 adjoint "
+                      f"scatter, {threads} threads), {len(times)} runs"}
 
 
 def run_reference(args):
