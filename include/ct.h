@@ -247,6 +247,63 @@ int ct_conv_transpose_nd_host(const void* x, const void* w, const void* bias,
                               int groups, int dtype, void* stream);
 
 /*
+ * Activations of the extended call, applied to each output after the bias
+ * and before the one rounding to the output type (the NKI page's
+ * conv3d_transpose activation_fn, "an optional activation applied after the
+ * convolution"; the page lists none, these are the common ones):
+ */
+typedef enum {
+    CT_ACT_NONE = 0,
+    CT_ACT_RELU = 1,        /* max(v, 0) */
+    CT_ACT_LEAKY_RELU = 2,  /* v >= 0 ? v : alpha * v */
+    CT_ACT_SILU = 3,        /* v / (1 + exp(-v)) */
+    CT_ACT_GELU = 4,        /* v * (1 + erf(v / sqrt(2))) / 2 */
+    CT_ACT_TANH = 5,
+    CT_ACT_SIGMOID = 6      /* 1 / (1 + exp(-v)) */
+} ct_activation;
+
+/* Weight layouts of the extended call (NKI page, conv3d_transpose filter_shape). */
+typedef enum {
+    CT_W_TORCH = 0,         /* [C_in, C_out/groups, k...] (PyTorch, ONNX) */
+    CT_W_KDHW_CI_CO = 1,    /* [k..., C_in, C_out], groups 1 */
+    CT_W_KDHW_CO_CI = 2     /* [k..., C_out, C_in], groups 1 */
+} ct_weight_layout;
+
+/*
+ * ct_conv_transpose_nd with the options of the NKI page's conv3d_transpose:
+ * w_layout (ct_weight_layout), taps_flipped (1: the stored taps are reversed
+ * along every spatial axis relative to the PyTorch orientation, i.e. the
+ * caller flipped them -- NKI's flip_filter_taps_in_kernel = False; 0: as
+ * PyTorch stores them), activation (ct_activation) and activation_alpha (the
+ * leaky-relu slope; ignored by the others).  A weight that is not in the
+ * PyTorch layout, or is flipped, is first rewritten into it in the head of
+ * the workspace (ct_conv_transpose_ex_workspace_bytes; NULL: allocated
+ * stream-ordered); the rest of the call is ct_conv_transpose_nd's, with the
+ * activation fused into every route's epilogue.  Extra errors: CT_ERR_PARAM
+ * for an unknown layout, flag or activation; CT_ERR_GROUPS for layouts 1, 2
+ * with groups != 1.
+ */
+int ct_conv_transpose_nd_ex(const void* x, const void* w, const void* bias,
+                            void* y, void* workspace, size_t workspace_bytes,
+                            int nd, int64_t B, int64_t C_in, int64_t C_out,
+                            const int64_t* in_spatial, const int64_t* k,
+                            const int* stride, const int* pad_lo,
+                            const int* pad_hi, const int* dilation,
+                            const int* output_padding, int groups, int dtype,
+                            int w_layout, int taps_flipped, int activation,
+                            float activation_alpha, void* stream);
+
+/* Workspace bytes of ct_conv_transpose_nd_ex for the given layout options. */
+int ct_conv_transpose_ex_workspace_bytes(int nd, int64_t B, int64_t C_in,
+                                         int64_t C_out, const int64_t* in_spatial,
+                                         const int64_t* k, const int* stride,
+                                         const int* pad_lo, const int* pad_hi,
+                                         const int* dilation,
+                                         const int* output_padding, int groups,
+                                         int dtype, int w_layout, int taps_flipped,
+                                         size_t* bytes);
+
+/*
  * Gradients of y = ConvTranspose(x, w, bias): the backward pass of the
  * SKaiNET pull request "feat(ops): implement convTranspose2d -- CPU kernel,
  * backward and StableHLO lowering" (#1464, Summary: convTranspose2dBackward,

@@ -438,3 +438,35 @@ int oracle_conv_transpose_backward_f64(const double* x, const double* w,
     pthread_mutex_destroy(&j.lock);
     return OR_OK;
 }
+
+/*
+ * Activation after the convolution, in fp64: the NKI page "Conv3D Transpose
+ * Kernel API Reference" (conv3d_transpose, activation_fn: an optional
+ * activation applied after the convolution).  The page does not list the
+ * functions; these are the common ones, each from its textbook definition:
+ *   0 none; 1 relu max(v, 0); 2 leaky relu v >= 0 ? v : alpha*v;
+ *   3 silu v / (1 + e^-v); 4 gelu v * (1 + erf(v / sqrt 2)) / 2;
+ *   5 tanh; 6 sigmoid 1 / (1 + e^-v).
+ * Applied in place to n values (y includes the bias).  Returns OR_OK or
+ * OR_BAD_ARG for an unknown code.
+ */
+#include <math.h>
+int oracle_activation_f64(double* y, int64_t n, int act, double alpha)
+{
+    if (act < 0 || act > 6) return OR_BAD_ARG;
+    for (int64_t e = 0; e < n; ++e) {
+        const double v = y[e];
+        double r = v;
+        switch (act) {
+            case 1: r = v > 0.0 ? v : 0.0; break;
+            case 2: r = v >= 0.0 ? v : alpha * v; break;
+            case 3: r = v / (1.0 + exp(-v)); break;
+            case 4: r = 0.5 * v * (1.0 + erf(v / sqrt(2.0))); break;
+            case 5: r = tanh(v); break;
+            case 6: r = 1.0 / (1.0 + exp(-v)); break;
+            default: break;
+        }
+        y[e] = r;
+    }
+    return OR_OK;
+}

@@ -40,7 +40,7 @@ def build(force: bool = False) -> str:
         tmp = _LIB + ".tmp%d" % os.getpid()
         subprocess.check_call([
             "gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
-            "-ffp-contract=off", "-o", tmp, _SRC])
+            "-ffp-contract=off", "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -59,6 +59,8 @@ def _lib():
         lib.oracle_conv_transpose_backward_f64.argtypes = (
             [_f64p] * 6 + [ctypes.c_int] + [ctypes.c_int64] * 4 + [_i64p] * 7
             + [ctypes.c_int])
+        lib.oracle_activation_f64.restype = ctypes.c_int
+        lib.oracle_activation_f64.argtypes = [_f64p, ctypes.c_int64, ctypes.c_int, ctypes.c_double]
         lib.oracle_points_f64.restype = ctypes.c_int
         lib.oracle_points_f64.argtypes = (
             [_f64p] * 3 + [ctypes.c_int] + [ctypes.c_int64] * 4 + [_i64p] * 7
@@ -222,3 +224,18 @@ def conv_transpose_backward(x, w, dy, stride=None, pad_lo=None, pad_hi=None,
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (code {rc})")
     return dx, dw, db
+
+
+ACTIVATIONS = {"none": 0, "relu": 1, "leaky_relu": 2, "silu": 3, "gelu": 4, "tanh": 5,
+               "sigmoid": 6}
+
+
+def activation(y, act, alpha=0.01):
+    """act(y) in float64 (a new array), as oracle_activation_f64 defines it:
+    the activation the NKI page applies after the convolution."""
+    code = ACTIVATIONS[act] if isinstance(act, str) else int(act)
+    out = np.ascontiguousarray(np.array(y, dtype=np.float64, copy=True))
+    rc = _lib().oracle_activation_f64(_fp(out), out.size, code, float(alpha))
+    if rc != 0:
+        raise ValueError(f"unknown activation {act!r}")
+    return out

@@ -171,3 +171,30 @@ def test_package_never_imports_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle", text, flags=re.M), f
                 assert "ct_oracle" not in text, f
+
+
+def test_extended_call_validates_its_options_before_launch(lib):
+    """ct_conv_transpose_nd_ex: unknown layout, flag or activation ->
+    CT_ERR_PARAM; the NKI layouts with groups != 1 -> CT_ERR_GROUPS; all
+    before any device work (CPU tensors stand in for the buffers)."""
+    x = torch.zeros((1, 4, 3))
+    w_nki = torch.zeros((2, 4, 6))   # [k, C_in, C_out]
+    y = torch.zeros((1, 6, 4))
+    cases = [(dict(w_layout=3), ctb.CT_ERR_PARAM),
+             (dict(taps_flipped=2), ctb.CT_ERR_PARAM),
+             (dict(activation=7), ctb.CT_ERR_PARAM),
+             (dict(activation=-1), ctb.CT_ERR_PARAM)]
+    for kw, want in cases:
+        args = dict(w_layout=ctb.CT_W_KDHW_CI_CO, taps_flipped=0, activation=0)
+        args.update(kw)
+        with pytest.raises(ctb.CtError) as e:
+            ctb.ct_conv_transpose_nd_ex(x, w_nki, None, y, stream=0, **args)
+        assert e.value.status == want, (kw, e.value)
+    with pytest.raises(ctb.CtError) as e:   # [k, C_in, C_out] with groups 2
+        ctb.ct_conv_transpose_nd_ex(x, w_nki, None, y, groups=2, w_layout=ctb.CT_W_KDHW_CI_CO,
+                                    stream=0)
+    assert e.value.status == ctb.CT_ERR_GROUPS
+    # workspace of a flipped PyTorch-layout weight: at least the weight's bytes
+    n = ctb.ct_conv_transpose_ex_workspace_bytes(1, 4, 6, [3], [2], [1], [0], [0], [1], [0],
+                                                 1, ctb.CT_F32, ctb.CT_W_TORCH, 1)
+    assert n >= 4 * 6 * 2 * 4

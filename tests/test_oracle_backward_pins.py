@@ -195,7 +195,7 @@ def _build_backward(tmp_path, text, name):
     so = tmp_path / f"{name}.so"
     c.write_text(text)
     subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", "-o",
-                           str(so), str(c)])
+                           str(so), str(c), "-lm"])
     f = ctypes.CDLL(str(so)).oracle_conv_transpose_backward_f64
     f.restype = ctypes.c_int
     f.argtypes = [_f64p] * 6 + [ctypes.c_int] + [ctypes.c_int64] * 4 + [_i64p] * 7 + [ctypes.c_int]

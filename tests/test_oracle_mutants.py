@@ -43,7 +43,7 @@ def _build(tmp_path, text, name):
     so = tmp_path / f"{name}.so"
     c.write_text(text)
     subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared",
-                           "-pthread", "-o", str(so), str(c)])
+                           "-pthread", "-o", str(so), str(c), "-lm"])
     lib = ctypes.CDLL(str(so))
     f = lib.oracle_conv_transpose_f64
     f.restype = ctypes.c_int

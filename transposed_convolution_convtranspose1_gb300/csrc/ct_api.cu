@@ -83,7 +83,7 @@ int fill_axes(Problem* p, int nd, const int64_t* in_spatial, const int64_t* k, c
 int validate(Problem* p, int nd, int64_t B, int64_t C_in, int64_t C_out, const int64_t* in_spatial,
              const int64_t* k, const int* stride, const int* pad_lo, const int* pad_hi,
              const int* dilation, const int* output_padding, int groups, int dtype) {
-    std::memset(p, 0, sizeof(*p));
+    *p = Problem{};
     int rc = fill_axes(p, nd, in_spatial, k, stride, pad_lo, pad_hi, dilation, output_padding);
     if (rc != CT_OK) return rc;
     if (dtype != CT_F32 && dtype != CT_F16 && dtype != CT_BF16)
@@ -332,7 +332,7 @@ int ct_conv_transpose_out_shape(int nd, const int64_t* in_spatial, const int64_t
                                 const int* dilation, const int* output_padding,
                                 int64_t* out_spatial) {
     Problem p;
-    std::memset(&p, 0, sizeof(p));
+    p = Problem{};
     int rc = fill_axes(&p, nd, in_spatial, k, stride, pad_lo, pad_hi, dilation, output_padding);
     if (rc != CT_OK) return rc;
     if (!out_spatial) return fail(CT_ERR_NULL, "out_spatial is NULL");
@@ -516,6 +516,86 @@ int ct_conv_transpose_nd_host(const void* x, const void* w, const void* bias, vo
     e = cudaStreamSynchronize(s);
     if (rc == CT_OK && e2 != cudaSuccess) rc = cuda_fail(e2, "ordering the host call's streams");
     if (rc == CT_OK && e != cudaSuccess) rc = cuda_fail(e, "cudaStreamSynchronize");
+    return rc;
+}
+
+// Options of the extended call: weight layout (0 PyTorch, 1 [k...][C_in][C_out],
+// 2 [k...][C_out][C_in]; 1 and 2 need groups == 1), taps stored reversed,
+// epilogue activation code (0..6) and its parameter.
+static int ex_options(Problem* p, int w_layout, int taps_flipped, int activation,
+                      float activation_alpha) {
+    if (w_layout < 0 || w_layout > 2) return fail(CT_ERR_PARAM, "w_layout must be 0, 1 or 2 (got %d)", w_layout);
+    if (w_layout != 0 && p->G != 1)
+        return fail(CT_ERR_GROUPS, "weight layouts 1 and 2 are defined for groups == 1 only");
+    if (taps_flipped != 0 && taps_flipped != 1) return fail(CT_ERR_PARAM, "taps_flipped must be 0 or 1");
+    if (activation < CT_ACT_NONE || activation > CT_ACT_SIGMOID)
+        return fail(CT_ERR_PARAM, "unknown activation %d", activation);
+    p->act = activation;
+    p->act_alpha = activation_alpha;
+    return CT_OK;
+}
+
+int ct_conv_transpose_ex_workspace_bytes(int nd, int64_t B, int64_t C_in, int64_t C_out,
+                                         const int64_t* in_spatial, const int64_t* k,
+                                         const int* stride, const int* pad_lo, const int* pad_hi,
+                                         const int* dilation, const int* output_padding,
+                                         int groups, int dtype, int w_layout, int taps_flipped,
+                                         size_t* bytes) {
+    if (!bytes) return fail(CT_ERR_NULL, "bytes is NULL");
+    Problem p;
+    int rc = validate(&p, nd, B, C_in, C_out, in_spatial, k, stride, pad_lo, pad_hi, dilation,
+                      output_padding, groups, dtype);
+    if (rc != CT_OK) return rc;
+    rc = ex_options(&p, w_layout, taps_flipped, CT_ACT_NONE, 0.f);
+    if (rc != CT_OK) return rc;
+    const bool conv = w_layout != 0 || taps_flipped != 0;
+    const size_t wb = conv ? ((size_t)p.w_elems() * p.elem_bytes() + 255) / 256 * 256 : 0;
+    *bytes = wb + route_workspace(p, choose_route(p));
+    return CT_OK;
+}
+
+int ct_conv_transpose_nd_ex(const void* x, const void* w, const void* bias, void* y,
+                            void* workspace, size_t workspace_bytes, int nd, int64_t B,
+                            int64_t C_in, int64_t C_out, const int64_t* in_spatial,
+                            const int64_t* k, const int* stride, const int* pad_lo,
+                            const int* pad_hi, const int* dilation, const int* output_padding,
+                            int groups, int dtype, int w_layout, int taps_flipped, int activation,
+                            float activation_alpha, void* stream) {
+    Problem p;
+    int rc = validate(&p, nd, B, C_in, C_out, in_spatial, k, stride, pad_lo, pad_hi, dilation,
+                      output_padding, groups, dtype);
+    if (rc != CT_OK) return rc;
+    rc = ex_options(&p, w_layout, taps_flipped, activation, activation_alpha);
+    if (rc != CT_OK) return rc;
+    rc = check_pointers(p, x, w, bias, y);
+    if (rc != CT_OK) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int route = choose_route(p);
+    const bool conv = w_layout != 0 || taps_flipped != 0;
+    if (!conv) return run(p, route, x, w, bias, y, workspace, workspace_bytes, s, nullptr);
+    // the weights in the PyTorch layout first, in the workspace's head
+    const size_t wb = ((size_t)p.w_elems() * p.elem_bytes() + 255) / 256 * 256;
+    const size_t need = wb + route_workspace(p, route);
+    char* ws = static_cast<char*>(workspace);
+    bool owned = false;
+    if (ws) {
+        if (workspace_bytes < need)
+            return fail(CT_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
+                        workspace_bytes, need);
+        if (!aligned(ws, 256)) return fail(CT_ERR_ALIGN, "workspace must be 256-byte aligned");
+    } else if (need > 0) {
+        cudaError_t e = cudaMallocAsync((void**)&ws, need, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(workspace)");
+        owned = true;
+    }
+    cudaError_t e = launch_weight_to_torch_layout(p, w, ws, w_layout, taps_flipped, s);
+    if (e != cudaSuccess) rc = cuda_fail(e, "weight layout kernel");
+    if (rc == CT_OK)
+        rc = run(p, route, x, ws, bias, y, need > wb ? ws + wb : nullptr, need - wb, s, nullptr);
+    if (owned) {
+        e = cudaFreeAsync(ws, s);
+        if (rc == CT_OK && e != cudaSuccess) rc = cuda_fail(e, "cudaFreeAsync(workspace)");
+    }
     return rc;
 }
 

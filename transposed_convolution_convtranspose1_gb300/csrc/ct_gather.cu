@@ -30,6 +30,8 @@ struct GatherArgs {
     int64_t In, On;
     int Kn;
     int64_t n_rows;  // B * G * n_ocb
+    int act;         // epilogue activation and its parameter
+    float act_alpha;
 };
 
 // Shared-memory weight slab layout: [tap][ic_g][j] (j = oc within the block).
@@ -115,17 +117,18 @@ __global__ void __launch_bounds__(128) gather_kernel(const GatherArgs a) {
         }
 #pragma unroll
         for (int j = 0; j < OCB; ++j)
-            if (j < nvalid) y[ybase + (int64_t)j * a.On + o] = from_f32<T>(acc[j] + bv[j]);
+            if (j < nvalid) y[ybase + (int64_t)j * a.On + o] = from_f32<T>(act_f32(acc[j] + bv[j], a.act, a.act_alpha));
     }
 }
 
 template <typename T>
 __global__ void bias_fill_kernel(const T* __restrict__ bias, T* __restrict__ y, int64_t C_out,
-                                 int64_t On, int64_t total) {
+                                 int64_t On, int64_t total, int act, float act_alpha) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t c = (i / On) % C_out;
-        y[i] = bias ? bias[c] : from_f32<T>(0.f);
+        const float v = bias ? to_f32(bias[c]) : 0.f;
+        y[i] = from_f32<T>(act_f32(v, act, act_alpha));
     }
 }
 
@@ -198,6 +201,8 @@ cudaError_t launch_gather(const Problem& p, const void* x, const void* w, const 
     a.In = p.in_spatial();
     a.On = p.out_spatial();
     a.Kn = (int)p.taps();
+    a.act = p.act;
+    a.act_alpha = p.act_alpha;
     switch (p.dtype) {
         case CT_F32: return launch_gather_dtype<float>(p, a, stream, prof);
         case CT_F16: return launch_gather_dtype<__half>(p, a, stream, prof);
@@ -220,19 +225,77 @@ cudaError_t launch_bias_fill(const Problem& p, const void* bias, void* y, cudaSt
     switch (p.dtype) {
         case CT_F32:
             bias_fill_kernel<float><<<(unsigned)blocks, threads, 0, stream>>>(
-                (const float*)bias, (float*)y, p.C_out, On, total);
+                (const float*)bias, (float*)y, p.C_out, On, total, p.act, p.act_alpha);
             break;
         case CT_F16:
             bias_fill_kernel<__half><<<(unsigned)blocks, threads, 0, stream>>>(
-                (const __half*)bias, (__half*)y, p.C_out, On, total);
+                (const __half*)bias, (__half*)y, p.C_out, On, total, p.act, p.act_alpha);
             break;
         default:
             bias_fill_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, stream>>>(
-                (const __nv_bfloat16*)bias, (__nv_bfloat16*)y, p.C_out, On, total);
+                (const __nv_bfloat16*)bias, (__nv_bfloat16*)y, p.C_out, On, total, p.act, p.act_alpha);
             break;
     }
     prof_end(prof, stream);
     prof_count(prof);
+    return cudaGetLastError();
+}
+
+// w in another layout -> w' in the PyTorch layout [C_in][C_out/groups][k...]
+// (the NKI page's filter_shape and flip_filter_taps_in_kernel, conv3d_transpose
+// parameters): layout 1 = [k...][C_in][C_out], layout 2 = [k...][C_out][C_in]
+// (groups 1), layout 0 = the PyTorch one; `flipped` means the stored taps are
+// reversed along every spatial axis.  One thread per element of w'.
+template <typename T>
+__global__ void weight_to_torch_layout(const T* __restrict__ w, T* __restrict__ wp, int64_t C_in,
+                                       int64_t Cog, int K0, int K1, int K2, int layout, int flipped,
+                                       int64_t total) {
+    const int64_t Kn = (int64_t)K0 * K1 * K2;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = e % Kn;
+        const int64_t oc = (e / Kn) % Cog;
+        const int64_t ic = e / (Kn * Cog);
+        int t2 = (int)(t % K2), t1 = (int)((t / K2) % K1), t0 = (int)(t / ((int64_t)K2 * K1));
+        if (flipped) {
+            t0 = K0 - 1 - t0;
+            t1 = K1 - 1 - t1;
+            t2 = K2 - 1 - t2;
+        }
+        const int64_t ts = ((int64_t)t0 * K1 + t1) * K2 + t2;
+        int64_t src;
+        if (layout == 1) src = (ts * C_in + ic) * Cog + oc;
+        else if (layout == 2) src = (ts * Cog + oc) * C_in + ic;
+        else src = (ic * Cog + oc) * Kn + ts;
+        wp[e] = w[src];
+    }
+}
+
+cudaError_t launch_weight_to_torch_layout(const Problem& p, const void* w, void* wp, int layout,
+                                          int flipped, cudaStream_t stream) {
+    const int64_t total = p.w_elems();
+    if (total == 0) return cudaSuccess;
+    DeviceInfo d;
+    cudaError_t e = device_info(&d);
+    if (e != cudaSuccess) return e;
+    const int threads = 256;
+    const int64_t blocks = std::min<int64_t>((total + threads - 1) / threads, (int64_t)d.sm_count * 8);
+    const int K0 = (int)p.K[0], K1 = (int)p.K[1], K2 = (int)p.K[2];
+    switch (p.dtype) {
+        case CT_F32:
+            weight_to_torch_layout<float><<<(unsigned)blocks, threads, 0, stream>>>(
+                (const float*)w, (float*)wp, p.C_in, p.Cog, K0, K1, K2, layout, flipped, total);
+            break;
+        case CT_F16:
+            weight_to_torch_layout<__half><<<(unsigned)blocks, threads, 0, stream>>>(
+                (const __half*)w, (__half*)wp, p.C_in, p.Cog, K0, K1, K2, layout, flipped, total);
+            break;
+        default:
+            weight_to_torch_layout<__nv_bfloat16><<<(unsigned)blocks, threads, 0, stream>>>(
+                (const __nv_bfloat16*)w, (__nv_bfloat16*)wp, p.C_in, p.Cog, K0, K1, K2, layout,
+                flipped, total);
+            break;
+    }
     return cudaGetLastError();
 }
 

@@ -26,6 +26,10 @@ struct Problem {
     int64_t I[3], K[3], O[3];
     int S[3], PL[3], PH[3], DL[3], OP[3];
     ct_dtype dtype;
+    // activation applied after the bias, before the one rounding to the
+    // output type (ct_activation codes; 0 = none) and its parameter
+    int act = 0;
+    float act_alpha = 0.f;
 
     int64_t in_spatial() const { return I[0] * I[1] * I[2]; }
     int64_t out_spatial() const { return O[0] * O[1] * O[2]; }
@@ -87,5 +91,9 @@ cudaError_t launch_bias_fill(const Problem& p, const void* bias, void* y,
                              cudaStream_t stream, Profile* prof);
 cudaError_t launch_gather(const Problem& p, const void* x, const void* w,
                           const void* bias, void* y, cudaStream_t stream, Profile* prof);
+// w in layout 1 ([k...][C_in][C_out]), 2 ([k...][C_out][C_in]) or 0 (the
+// PyTorch layout), taps reversed when `flipped` -> wp in the PyTorch layout.
+cudaError_t launch_weight_to_torch_layout(const Problem& p, const void* w, void* wp, int layout,
+                                          int flipped, cudaStream_t stream);
 
 }  // namespace ct

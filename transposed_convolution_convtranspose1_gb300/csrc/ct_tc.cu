@@ -100,6 +100,8 @@ struct TcParams {
     int vec_store;        // 16-byte output stores allowed (O_w % 8 == 0, y aligned)
     int tma_store;        // SW = 2: epilogue writes 32 channels x 64 outputs per tensor store
     uint32_t epi_off;     // offset of the per-warp 4 KiB staging buffers from the ring
+    int act;              // epilogue activation and its parameter
+    float act_alpha;
 };
 
 // ---------------------------------------------------------------------------
@@ -411,8 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                     }
 #pragma unroll
                     for (int i = 0; i < Sh::CQ / 2; ++i)
-                        held[st][c * (Sh::CQ / 2) + i] = bits16(from_f32<T>(v[2 * i] + bv)) |
-                                                         (bits16(from_f32<T>(v[2 * i + 1] + bv)) << 16);
+                        held[st][c * (Sh::CQ / 2) + i] = bits16(from_f32<T>(act_f32(v[2 * i] + bv, P.act, P.act_alpha))) |
+                                                         (bits16(from_f32<T>(act_f32(v[2 * i + 1] + bv, P.act, P.act_alpha))) << 16);
                 }
                 if (work) {
                     tc_fence_before();
@@ -461,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                                     const int qi = pc * 4 + hh;  // outputs 2qi (phase 0), 2qi+1
                                     const uint32_t w2 = held[0][c * (Sh::CQ / 2) + qi / 2];
                                     const uint32_t h16 = (qi & 1) ? (w2 >> 16) : (w2 & 0xFFFFu);
-                                    const uint32_t v16 = bits16(from_f32<T>(v[qi] + bv));
+                                    const uint32_t v16 = bits16(from_f32<T>(act_f32(v[qi] + bv, P.act, P.act_alpha)));
                                     wv[hh] = rl == 1 ? (h16 | (v16 << 16)) : (v16 | (h16 << 16));
                                 }
                                 const uint32_t a = sbuf + lane * 128 + ((pc ^ (lane & 7)) << 4);
@@ -490,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                                 const int j = pc * 8 + hh * 2 + e;
                                 const int qi = j / SW, r = j % SW;
                                 if (r == rl) {
-                                    two[e] = bits16(from_f32<T>(v[qi] + bv));
+                                    two[e] = bits16(from_f32<T>(act_f32(v[qi] + bv, P.act, P.act_alpha)));
                                 } else {
                                     // held step of residue r: 0 for SW = 2, r otherwise
                                     const int hs = SW == 2 ? 0 : (r < SW - 1 ? r : 0);
@@ -734,6 +736,8 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
     TcParams P;
     std::memset(&P, 0, sizeof(P));
     P.bias = bias;
+    P.act = p.act;
+    P.act_alpha = p.act_alpha;
     P.y = y;
     P.C_out = (int)p.C_out;
     P.n_kblk = pl.C_pad / kBlockK;

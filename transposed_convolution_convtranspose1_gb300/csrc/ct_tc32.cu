@@ -56,6 +56,7 @@
 
 #include "ct_routes.h"
 #include "ct_tcgen05.cuh"
+#include "ct_types.cuh"
 
 namespace ct {
 
@@ -107,6 +108,8 @@ struct Tc32Params {
     uint32_t idesc_half;    // N = kNP / 2 (half tiles)
     uint32_t tmem_cols;
     uint32_t epi_off;       // offset of the epilogue blocks from the ring
+    int act;                // epilogue activation and its parameter
+    float act_alpha;
 };
 
 struct Tile {
@@ -399,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
                 if (!group_valid(c, qh, qwb)) continue;  // warp-uniform
                 // lane = channel: row `lane` of the block
 #pragma unroll
-                for (int i = 0; i < 32; ++i) stg[lane * 32 + (i ^ lane)] = acc[c * 32 + i] + bv;
+                for (int i = 0; i < 32; ++i) stg[lane * 32 + (i ^ lane)] = act_f32(acc[c * 32 + i] + bv, P.act, P.act_alpha);
                 __syncwarp();
                 // lane = position: column `lane`, one output row per channel
                 const int oh = C.rh + P.S[1] * qh;
@@ -641,6 +644,8 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
     P.stages = pl.stages;
     P.stage_bytes = (uint32_t)pl.stage_bytes;
     P.tmem_cols = 2 * kNP;
+    P.act = p.act;
+    P.act_alpha = p.act_alpha;
     P.idesc = (1u << 4)                              // D = f32
               | (2u << 7)                            // A = tf32
               | (2u << 10)                           // B = tf32

@@ -34,4 +34,20 @@ __device__ __forceinline__ void fma2(float2& d, const float2 a, const float2 b) 
     d.y = __uint_as_float((unsigned)(ud >> 32));
 }
 
+// Activation of the epilogue (ct_activation codes of include/ct.h), applied
+// to the fp32 value after the bias and before the one rounding to the
+// output type: 1 relu, 2 leaky relu (alpha), 3 silu, 4 gelu (erf form),
+// 5 tanh, 6 sigmoid; anything else leaves v unchanged.
+__device__ __forceinline__ float act_f32(float v, int act, float alpha) {
+    switch (act) {
+        case 1: return v > 0.f ? v : 0.f;
+        case 2: return v >= 0.f ? v : alpha * v;
+        case 3: return v / (1.f + expf(-v));
+        case 4: return 0.5f * v * (1.f + erff(v * 0.70710678118654752f));
+        case 5: return tanhf(v);
+        case 6: return 1.f / (1.f + expf(-v));
+        default: return v;
+    }
+}
+
 }  // namespace ct

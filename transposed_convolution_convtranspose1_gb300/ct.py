@@ -49,10 +49,19 @@ EXPORTS = ("ct_version", "ct_last_error", "ct_status_string",
            "ct_conv_transpose_nd", "ct_conv_transpose_nd_route",
            "ct_conv_transpose_nd_host", "ct_conv_transpose_nd_profiled",
            "ct_conv_transpose_nd_noalloc", "ct_device_status", "ct_host_buffers_release",
-           "ct_conv_transpose_backward_nd", "ct_conv_transpose_backward_workspace_bytes")
+           "ct_conv_transpose_backward_nd", "ct_conv_transpose_backward_workspace_bytes",
+           "ct_conv_transpose_nd_ex", "ct_conv_transpose_ex_workspace_bytes")
 
 # Size of the static scratch behind ct_conv_transpose_nd_noalloc (CT_NOALLOC_SCRATCH_BYTES).
 CT_NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+# ct_activation and ct_weight_layout (include/ct.h)
+CT_ACT_NONE, CT_ACT_RELU, CT_ACT_LEAKY_RELU, CT_ACT_SILU = 0, 1, 2, 3
+CT_ACT_GELU, CT_ACT_TANH, CT_ACT_SIGMOID = 4, 5, 6
+ACTIVATIONS = {"none": 0, "relu": 1, "leaky_relu": 2, "silu": 3, "gelu": 4, "tanh": 5,
+               "sigmoid": 6}
+CT_W_TORCH, CT_W_KDHW_CI_CO, CT_W_KDHW_CO_CI = 0, 1, 2
 
 
 class CtError(RuntimeError):
@@ -109,6 +118,13 @@ def _declare(h):
     h.ct_device_status.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_uint)]
     h.ct_host_buffers_release.restype = ctypes.c_int
     h.ct_host_buffers_release.argtypes = []
+    h.ct_conv_transpose_nd_ex.restype = ctypes.c_int
+    h.ct_conv_transpose_nd_ex.argtypes = ([_vp, _vp, _vp, _vp, _vp, ctypes.c_size_t] + _SHAPE_ARGS
+                                          + [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_float, _vp])
+    h.ct_conv_transpose_ex_workspace_bytes.restype = ctypes.c_int
+    h.ct_conv_transpose_ex_workspace_bytes.argtypes = _SHAPE_ARGS + [
+        ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
     h.ct_conv_transpose_backward_nd.restype = ctypes.c_int
     h.ct_conv_transpose_backward_nd.argtypes = ([_vp] * 7 + [ctypes.c_size_t] + _SHAPE_ARGS + [_vp])
     h.ct_conv_transpose_backward_workspace_bytes.restype = ctypes.c_int
@@ -433,4 +449,47 @@ def conv_transpose_autograd(x, w, bias=None, stride=1, padding=0, pad_lo=None, p
     """conv_transpose that records itself for torch.autograd."""
     return ConvTransposeFunction.apply(x, w, bias, stride, padding, pad_lo, pad_hi, dilation,
                                        output_padding, groups)
+
+
+def _problem_ex(x, w, groups, w_layout):
+    """(nd, B, C_in, C_out, I, K) for a weight in any ct_weight_layout."""
+    if w_layout == CT_W_TORCH:
+        return _problem_from_tensors(x, w, groups)
+    nd = x.dim() - 2
+    if nd < 1 or w.dim() != x.dim():
+        raise CtError(CT_ERR_RANK, "x must be [B, C_in, *spatial] and w [*k, C_in, C_out] "
+                                   "or [*k, C_out, C_in]")
+    C_out = w.shape[-1] if w_layout == CT_W_KDHW_CI_CO else w.shape[-2]
+    return nd, x.shape[0], x.shape[1], C_out, tuple(x.shape[2:]), tuple(w.shape[:nd])
+
+
+def ct_conv_transpose_ex_workspace_bytes(B, C_in, C_out, in_spatial, k, stride=None, pad_lo=None,
+                                         pad_hi=None, dilation=None, output_padding=None,
+                                         groups=1, dtype=CT_F32, w_layout=CT_W_TORCH,
+                                         taps_flipped=0) -> int:
+    ax = _Axes(len(in_spatial), in_spatial, k, stride, pad_lo, pad_hi, dilation, output_padding)
+    n = ctypes.c_size_t(0)
+    _check(lib().ct_conv_transpose_ex_workspace_bytes(
+        *_shape_args(B, C_in, C_out, ax, groups, dtype), int(w_layout), int(taps_flipped),
+        ctypes.byref(n)))
+    return int(n.value)
+
+
+def ct_conv_transpose_nd_ex(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
+                            y: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+                            stride=None, pad_lo=None, pad_hi=None, dilation=None,
+                            output_padding=None, groups: int = 1, w_layout: int = CT_W_TORCH,
+                            taps_flipped: int = 0, activation=CT_ACT_NONE,
+                            activation_alpha: float = 0.01, stream=None) -> None:
+    """Run the extended entry point (weight layout, flipped taps, fused
+    activation) on torch CUDA tensors; y is overwritten."""
+    nd, B, C_in, C_out, I, K = _problem_ex(x, w, groups, w_layout)
+    act = ACTIVATIONS[activation] if isinstance(activation, str) else int(activation)
+    ax = _Axes(nd, I, K, stride, pad_lo, pad_hi, dilation, output_padding)
+    nws = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    s = _stream_handle(stream, x.device)
+    _check(lib().ct_conv_transpose_nd_ex(
+        _ptr(x), _ptr(w), _ptr(bias), _ptr(y), _ptr(workspace), nws,
+        *_shape_args(B, C_in, C_out, ax, groups, dtype_code(x.dtype)), int(w_layout),
+        int(taps_flipped), act, float(activation_alpha), s))
 
