@@ -170,6 +170,11 @@ int run(const Problem& p, int route, const void* x, const void* w, const void* b
         case CT_ROUTE_TC32_GEMM: e = launch_tc32(p, x, w, bias, y, ws, stream, prof); break;
         default: e = cudaErrorInvalidValue; break;
     }
+    // the CUDA-core routes apply an activation as a second pass over y (the
+    // tcgen05 routes and the bias fill fuse it into their epilogues)
+    if (e == cudaSuccess && p.act != 0 &&
+        (route == CT_ROUTE_GATHER || route == CT_ROUTE_GROUPED || route == CT_ROUTE_SIMT_GEMM))
+        e = launch_activation(p, y, stream, prof);
     if (owned) {
         cudaError_t e2 = cudaFreeAsync(ws, stream);
         if (e == cudaSuccess) e = e2;

@@ -30,8 +30,6 @@ struct GatherArgs {
     int64_t In, On;
     int Kn;
     int64_t n_rows;  // B * G * n_ocb
-    int act;         // epilogue activation and its parameter
-    float act_alpha;
 };
 
 // Shared-memory weight slab layout: [tap][ic_g][j] (j = oc within the block).
@@ -117,7 +115,7 @@ __global__ void __launch_bounds__(128) gather_kernel(const GatherArgs a) {
         }
 #pragma unroll
         for (int j = 0; j < OCB; ++j)
-            if (j < nvalid) y[ybase + (int64_t)j * a.On + o] = from_f32<T>(act_f32(acc[j] + bv[j], a.act, a.act_alpha));
+            if (j < nvalid) y[ybase + (int64_t)j * a.On + o] = from_f32<T>(acc[j] + bv[j]);
     }
 }
 
@@ -201,8 +199,6 @@ cudaError_t launch_gather(const Problem& p, const void* x, const void* w, const 
     a.In = p.in_spatial();
     a.On = p.out_spatial();
     a.Kn = (int)p.taps();
-    a.act = p.act;
-    a.act_alpha = p.act_alpha;
     switch (p.dtype) {
         case CT_F32: return launch_gather_dtype<float>(p, a, stream, prof);
         case CT_F16: return launch_gather_dtype<__half>(p, a, stream, prof);
@@ -296,6 +292,41 @@ cudaError_t launch_weight_to_torch_layout(const Problem& p, const void* w, void*
                 flipped, total);
             break;
     }
+    return cudaGetLastError();
+}
+
+// y = act(y) in place: the activation of the CUDA-core routes (gather,
+// grouped, SIMT), whose unrolled epilogues would carry the activation's code
+// at every store site; it runs as a second pass over y (16-bit outputs are
+// then rounded twice).
+template <typename T>
+__global__ void activation_kernel(T* __restrict__ y, int64_t n, int act, float alpha) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        y[i] = from_f32<T>(act_f32(to_f32(y[i]), act, alpha));
+}
+
+cudaError_t launch_activation(const Problem& p, void* y, cudaStream_t stream, Profile* prof) {
+    const int64_t n = p.y_elems();
+    if (n == 0 || p.act == 0) return cudaSuccess;
+    DeviceInfo d;
+    cudaError_t e = device_info(&d);
+    if (e != cudaSuccess) return e;
+    const int threads = 256;
+    const int64_t blocks = std::min<int64_t>((n + threads - 1) / threads, (int64_t)d.sm_count * 16);
+    switch (p.dtype) {
+        case CT_F32:
+            activation_kernel<float><<<(unsigned)blocks, threads, 0, stream>>>((float*)y, n, p.act, p.act_alpha);
+            break;
+        case CT_F16:
+            activation_kernel<__half><<<(unsigned)blocks, threads, 0, stream>>>((__half*)y, n, p.act, p.act_alpha);
+            break;
+        default:
+            activation_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, stream>>>(
+                (__nv_bfloat16*)y, n, p.act, p.act_alpha);
+            break;
+    }
+    prof_count(prof);
     return cudaGetLastError();
 }
 

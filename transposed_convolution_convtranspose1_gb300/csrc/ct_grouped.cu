@@ -57,8 +57,6 @@ struct GroupedParams {
     int vec2;              // fp32, stride 2 along W: rows 8-byte aligned (float2 stores)
     int cigp;              // staged variant: channels per group padded to 4, 8 or 16
     int ws, base_w;        // staged row: WS positions p, iw = p + base_w
-    int act;               // epilogue activation and its parameter
-    float act_alpha;
 };
 
 // slab layout: [tap][ic][COG] (COG >= Cog, zero padded)
@@ -147,7 +145,7 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_kernel(const __grid_co
 #pragma unroll
             for (int r = 0; r < SW; ++r)
                 if (q < P.qw_ext[r])
-                    yrow[(int64_t)oc * out_plane + r + (int64_t)SW * q] = from_f32<T>(act_f32(acc[r][oc] + bv[oc], P.act, P.act_alpha));
+                    yrow[(int64_t)oc * out_plane + r + (int64_t)SW * q] = from_f32<T>(acc[r][oc] + bv[oc]);
         }
     }
 }
@@ -326,14 +324,14 @@ __global__ void __launch_bounds__(kGrpWarps * 32) grouped_staged_kernel(const __
                         if (P.vec2 && q < P.qw_ext[1]) {
                             const float v0 = (oc & 1) ? acc[u][0][oc >> 1].y : acc[u][0][oc >> 1].x;
                             const float v1 = (oc & 1) ? acc[u][1][oc >> 1].y : acc[u][1][oc >> 1].x;
-                            *reinterpret_cast<float2*>(yo) = make_float2(act_f32(v0 + bo, P.act, P.act_alpha), act_f32(v1 + bo, P.act, P.act_alpha));
+                            *reinterpret_cast<float2*>(yo) = make_float2(v0 + bo, v1 + bo);
                             continue;
                         }
                     }
 #pragma unroll
                     for (int r = 0; r < SW; ++r) {
                         const float v = (oc & 1) ? acc[u][r][oc >> 1].y : acc[u][r][oc >> 1].x;
-                        if (q < P.qw_ext[r]) yo[r] = from_f32<T>(act_f32(v + bo, P.act, P.act_alpha));
+                        if (q < P.qw_ext[r]) yo[r] = from_f32<T>(v + bo);
                     }
                 }
             }
@@ -484,8 +482,6 @@ cudaError_t launch_grouped(const Problem& p, const void* x, const void* w, const
     P.y = y;
     P.C_in = (int)p.C_in;
     P.C_out = (int)p.C_out;
-    P.act = p.act;
-    P.act_alpha = p.act_alpha;
     P.G = p.G;
     P.Cig = p.Cig;
     P.Cog = p.Cog;

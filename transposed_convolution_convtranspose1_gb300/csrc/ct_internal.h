@@ -91,6 +91,8 @@ cudaError_t launch_bias_fill(const Problem& p, const void* bias, void* y,
                              cudaStream_t stream, Profile* prof);
 cudaError_t launch_gather(const Problem& p, const void* x, const void* w,
                           const void* bias, void* y, cudaStream_t stream, Profile* prof);
+// y = act(y) in place (Problem.act), for the routes without a fused one.
+cudaError_t launch_activation(const Problem& p, void* y, cudaStream_t stream, Profile* prof);
 // w in layout 1 ([k...][C_in][C_out]), 2 ([k...][C_out][C_in]) or 0 (the
 // PyTorch layout), taps reversed when `flipped` -> wp in the PyTorch layout.
 cudaError_t launch_weight_to_torch_layout(const Problem& p, const void* w, void* wp, int layout,

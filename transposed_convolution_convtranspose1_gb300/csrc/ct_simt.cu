@@ -46,8 +46,6 @@ struct SimtParams {
     int qw_ext[kSimtMaxS];
     int n_qblk, n_ocblk;
     int64_t n_blocks;
-    int act;                // epilogue activation and its parameter
-    float act_alpha;
 };
 
 __device__ __forceinline__ void cp_async16(float* dst, const float* src) {
@@ -191,7 +189,7 @@ __global__ void __launch_bounds__(kSimtThreads, 2) simt_phase_gemm(const __grid_
         for (int j = 0; j < 8; ++j) {
             const int q = q0 + tx * 4 + (j & 3) + (j >> 2) * 64;
             const float a = (j & 1) ? acc2[i][j >> 1].y : acc2[i][j >> 1].x;
-            if (q < qext) yr[rw + (int64_t)P.S[2] * q] = act_f32(a + bv, P.act, P.act_alpha);
+            if (q < qext) yr[rw + (int64_t)P.S[2] * q] = a + bv;
         }
     }
 }
@@ -267,8 +265,6 @@ cudaError_t launch_simt(const Problem& p, const void* x, const void* w, const vo
     P.x = static_cast<const float*>(x);
     P.wp = wp;
     P.bias = static_cast<const float*>(bias);
-    P.act = p.act;
-    P.act_alpha = p.act_alpha;
     P.y = static_cast<float*>(y);
     P.C_in = (int)p.C_in;
     P.C_in_pad = pl.C_in_pad;

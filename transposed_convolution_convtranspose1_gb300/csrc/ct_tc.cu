@@ -197,7 +197,15 @@ __device__ __forceinline__ uint32_t bits16(__half v) { return *reinterpret_cast<
 // stored while the next tile's first phases run.
 // ---------------------------------------------------------------------------
 
-template <typename T, int SW>
+// The epilogue's activation is a compile-time choice (ACT): the plain kernel
+// carries no trace of it.
+template <bool ACT>
+__device__ __forceinline__ float epi_act(float v, const TcParams& P) {
+    if constexpr (ACT) return act_f32(v, P.act, P.act_alpha);
+    else return v;
+}
+
+template <typename T, int SW, bool ACT>
 __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_constant__ TcParams P) {
     using Sh = TcShape<SW>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -413,8 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                     }
 #pragma unroll
                     for (int i = 0; i < Sh::CQ / 2; ++i)
-                        held[st][c * (Sh::CQ / 2) + i] = bits16(from_f32<T>(act_f32(v[2 * i] + bv, P.act, P.act_alpha))) |
-                                                         (bits16(from_f32<T>(act_f32(v[2 * i + 1] + bv, P.act, P.act_alpha))) << 16);
+                        held[st][c * (Sh::CQ / 2) + i] = bits16(from_f32<T>(epi_act<ACT>(v[2 * i] + bv, P))) |
+                                                         (bits16(from_f32<T>(epi_act<ACT>(v[2 * i + 1] + bv, P))) << 16);
                 }
                 if (work) {
                     tc_fence_before();
@@ -463,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                                     const int qi = pc * 4 + hh;  // outputs 2qi (phase 0), 2qi+1
                                     const uint32_t w2 = held[0][c * (Sh::CQ / 2) + qi / 2];
                                     const uint32_t h16 = (qi & 1) ? (w2 >> 16) : (w2 & 0xFFFFu);
-                                    const uint32_t v16 = bits16(from_f32<T>(act_f32(v[qi] + bv, P.act, P.act_alpha)));
+                                    const uint32_t v16 = bits16(from_f32<T>(epi_act<ACT>(v[qi] + bv, P)));
                                     wv[hh] = rl == 1 ? (h16 | (v16 << 16)) : (v16 | (h16 << 16));
                                 }
                                 const uint32_t a = sbuf + lane * 128 + ((pc ^ (lane & 7)) << 4);
@@ -492,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                                 const int j = pc * 8 + hh * 2 + e;
                                 const int qi = j / SW, r = j % SW;
                                 if (r == rl) {
-                                    two[e] = bits16(from_f32<T>(act_f32(v[qi] + bv, P.act, P.act_alpha)));
+                                    two[e] = bits16(from_f32<T>(epi_act<ACT>(v[qi] + bv, P)));
                                 } else {
                                     // held step of residue r: 0 for SW = 2, r otherwise
                                     const int hs = SW == 2 ? 0 : (r < SW - 1 ? r : 0);
@@ -700,9 +708,9 @@ bool make_plan(const Problem& p, TcPlan* pl) {
     return true;
 }
 
-template <typename T, int SW>
-cudaError_t launch_gemm(const TcParams& P, int grid, size_t smem, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(tc_phase_gemm<T, SW>,
+template <typename T, int SW, bool ACT>
+cudaError_t launch_gemm_t(const TcParams& P, int grid, size_t smem, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(tc_phase_gemm<T, SW, ACT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // Programmatic dependent launch: the GEMM's CTAs may start (barrier
@@ -718,7 +726,13 @@ cudaError_t launch_gemm(const TcParams& P, int grid, size_t smem, cudaStream_t s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_phase_gemm<T, SW>, P);
+    return cudaLaunchKernelEx(&cfg, tc_phase_gemm<T, SW, ACT>, P);
+}
+
+template <typename T, int SW>
+cudaError_t launch_gemm(const TcParams& P, int grid, size_t smem, cudaStream_t stream) {
+    return P.act != 0 ? launch_gemm_t<T, SW, true>(P, grid, smem, stream)
+                      : launch_gemm_t<T, SW, false>(P, grid, smem, stream);
 }
 
 template <typename T>

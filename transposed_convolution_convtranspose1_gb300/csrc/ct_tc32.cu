@@ -171,6 +171,9 @@ __device__ __forceinline__ int tile_at(int k) {
 // the GEMM kernel
 // ---------------------------------------------------------------------------
 
+// The epilogue's activation is a compile-time choice (ACT): the plain kernel
+// carries no trace of it.
+template <bool ACT>
 __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_constant__ Tc32Params P) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint64_t full_bar[8], empty_bar[8], sfull_bar[2], sempty_bar[2], drain_bar;
@@ -402,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
                 if (!group_valid(c, qh, qwb)) continue;  // warp-uniform
                 // lane = channel: row `lane` of the block
 #pragma unroll
-                for (int i = 0; i < 32; ++i) stg[lane * 32 + (i ^ lane)] = act_f32(acc[c * 32 + i] + bv, P.act, P.act_alpha);
+                for (int i = 0; i < 32; ++i) stg[lane * 32 + (i ^ lane)] = (ACT ? act_f32(acc[c * 32 + i] + bv, P.act, P.act_alpha) : acc[c * 32 + i] + bv);
                 __syncwarp();
                 // lane = position: column `lane`, one output row per channel
                 const int oh = C.rh + P.S[1] * qh;
@@ -754,7 +757,8 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
     }
     const size_t smem = (size_t)P.stages * P.stage_bytes + pl.epi_bytes + 1024;
     const int grid = std::max(1, std::min(P.total_slots, dev.sm_count));
-    e = cudaFuncSetAttribute(tc32_phase_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(P.act != 0 ? tc32_phase_gemm<true> : tc32_phase_gemm<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     prof_begin(prof, stream);
     {
@@ -772,7 +776,8 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, tc32_phase_gemm, P);
+        e = P.act != 0 ? cudaLaunchKernelEx(&cfg, tc32_phase_gemm<true>, P)
+                       : cudaLaunchKernelEx(&cfg, tc32_phase_gemm<false>, P);
     }
     prof_end(prof, stream);
     prof_count(prof);
