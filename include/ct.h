@@ -248,9 +248,12 @@ int ct_conv_transpose_nd_host(const void* x, const void* w, const void* bias,
 
 /*
  * Activations of the extended call, applied to each output after the bias
- * and before the one rounding to the output type (the NKI page's
- * conv3d_transpose activation_fn, "an optional activation applied after the
- * convolution"; the page lists none, these are the common ones):
+ * (the NKI page's conv3d_transpose takes an optional activation function
+ * run on the convolution's result; it names no particular ones, so these are
+ * the common ones).  The tcgen05 routes and the bias fill apply it in fp32
+ * before the one rounding to the output type; the CUDA-core routes (gather,
+ * grouped, SIMT) round the convolution first and apply it in a second pass
+ * over y, so a 16-bit output is then rounded twice.
  */
 typedef enum {
     CT_ACT_NONE = 0,
@@ -278,8 +281,8 @@ typedef enum {
  * leaky-relu slope; ignored by the others).  A weight that is not in the
  * PyTorch layout, or is flipped, is first rewritten into it in the head of
  * the workspace (ct_conv_transpose_ex_workspace_bytes; NULL: allocated
- * stream-ordered); the rest of the call is ct_conv_transpose_nd's, with the
- * activation fused into every route's epilogue.  Extra errors: CT_ERR_PARAM
+ * stream-ordered); the rest of the call is ct_conv_transpose_nd's, followed
+ * by the activation as described at ct_activation.  Extra errors: CT_ERR_PARAM
  * for an unknown layout, flag or activation; CT_ERR_GROUPS for layouts 1, 2
  * with groups != 1.
  */

@@ -26,8 +26,9 @@ struct Problem {
     int64_t I[3], K[3], O[3];
     int S[3], PL[3], PH[3], DL[3], OP[3];
     ct_dtype dtype;
-    // activation applied after the bias, before the one rounding to the
-    // output type (ct_activation codes; 0 = none) and its parameter
+    // activation applied after the bias (ct_activation codes; 0 = none) and
+    // its parameter: fused by the tcgen05 routes and the bias fill, a second
+    // pass over y (launch_activation) on the CUDA-core routes
     int act = 0;
     float act_alpha = 0.f;
 

@@ -34,9 +34,8 @@ __device__ __forceinline__ void fma2(float2& d, const float2 a, const float2 b) 
     d.y = __uint_as_float((unsigned)(ud >> 32));
 }
 
-// Activation of the epilogue (ct_activation codes of include/ct.h), applied
-// to the fp32 value after the bias and before the one rounding to the
-// output type: 1 relu, 2 leaky relu (alpha), 3 silu, 4 gelu (erf form),
+// Activation (ct_activation codes of include/ct.h) of an fp32 value after
+// the bias: 1 relu, 2 leaky relu (alpha), 3 silu, 4 gelu (erf form),
 // 5 tanh, 6 sigmoid; anything else leaves v unchanged.
 __device__ __forceinline__ float act_f32(float v, int act, float alpha) {
     switch (act) {
