@@ -54,8 +54,9 @@
 extern "C" {
 #endif
 
-/* Element types.  Integer types are not accepted ("dtype guard so non-float
- * dtypes fail loudly", SKaiNET #1464, Summary). */
+/* Element types.  Integer types are not accepted: the SKaiNET pull request
+ * (#1464, Summary) rejects non-float dtypes with an error instead of
+ * computing with them. */
 typedef enum { CT_F32 = 0, CT_F16 = 1, CT_BF16 = 2 } ct_dtype;
 
 typedef enum {

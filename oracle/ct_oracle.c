@@ -13,8 +13,8 @@
  * every input sample is multiplied by every weight tap and added into the
  * output position  i*stride - padding + t*dilation  of each axis, and products
  * that land outside the output are dropped.  The same page states the PyTorch
- * conventions used here: weight layout [C_in, C_out/groups, k...] and a
- * groups-aware C_out = w.shape[1] * groups.  The ONNX page "ai.onnx.ConvTranspose"
+ * conventions used here: weight layout [C_in, C_out/groups, k...], so the
+ * output channel count is C_out = w.shape[1] * groups.  The ONNX page "ai.onnx.ConvTranspose"
  * (Description) and the NKI page "Conv3D Transpose Kernel API Reference"
  * (conv3d_transpose parameters) extend it to 1-D/3-D, asymmetric low/high
  * padding and output_padding on the high side.

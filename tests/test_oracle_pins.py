@@ -3,7 +3,9 @@
 None of these re-types the oracle's own formula.  They check it against
 - output shapes the pages and workloads state (tests/golden/out_shapes.json),
 - the two hand-computed cases named in the SKaiNET pull request's test list
-  (k2/s1 full scatter, k2/s2 non-overlapping stamp), in closed form,
+  (kernel 2 at stride 1, where every tap overlaps its neighbours, and
+  kernel 2 at stride 2, where the taps tile the output without overlap), in
+  closed form,
 - library routines: scipy's full N-D convolution (stride 1, no padding),
   torch.nn.functional.conv_transposeNd and convNd in float64,
 - the forward-convolution equivalence the pages use (input dilated by the

@@ -5,12 +5,11 @@
 // [0, I) on every axis -- the scatter of SKaiNET #1464 (Summary, DefaultCpuOps)
 // with its index map inverted, so that each thread owns its outputs and no two
 // threads add into the same element (no atomics).  One thread owns one
-// output position and a block of OCB output channels of one group, in the
-// manner of the ONNX page's grouped stride-phase variant (one invocation owns
-// one output pixel and a block of its group's output channels, every gathered
-// input sample feeds the whole block, the group's weight slab is staged once
-// per workgroup).  This kernel serves every shape and dtype and is the
-// reference route the specialised routes are tested beside.
+// output position and a block of OCB output channels of one group, as in
+// the ONNX page's grouped stride-phase variant: each input value it reads is
+// used for all OCB channels, and the block keeps the group's weights in
+// shared memory, loaded a single time.  This kernel serves every shape and
+// dtype and is the reference route the specialised routes are tested beside.
 #include <algorithm>
 
 #include "ct_internal.h"

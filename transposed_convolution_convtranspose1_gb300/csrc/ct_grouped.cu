@@ -1,9 +1,10 @@
 // ct_grouped.cu -- grouped/depthwise stride-phase gather on CUDA cores.
 //
 // The ONNX page's grouped stride-phase variant (ai.onnx.ConvTranspose,
-// nchw2d_grouped_stride_phase_blocked): one invocation owns output pixels and
-// the whole block of its group's output channels, every gathered input sample
-// feeds that block, and the group's weight slab is staged once per workgroup.
+// nchw2d_grouped_stride_phase_blocked): a thread computes some output
+// positions for all output channels of their group, so each input value read
+// serves every one of those channels, and a block loads its group's weights
+// into shared memory a single time.
 // Laid out for GB300:
 //   - one warp per output row (b, od, oh), so every lane shares the row's D
 //     and H residues and therefore its tap lists (no divergence on them);
