@@ -6,7 +6,10 @@ The problems cover: the grouped workload's geometry (one live W residue:
 1 and 3, odd output widths, input rows wider than the staged kernel's span
 (direct kernel), ragged bands along H, mixed strides with dilation and
 asymmetric pads, a 3-D output with a D stride, no bias, 16-bit dtypes, and
-an output that is only 4-byte aligned (2-wide stores off).
+an output that is only 4-byte aligned (2-wide stores off).  The fp32 problems
+whose input width is a multiple of 4 take the kernel whose input rows arrive
+by TMA boxes (channel boxes past the last channel, rows and columns outside
+the input read as zero).
 """
 import numpy as np
 import pytest
@@ -52,6 +55,16 @@ SHAPES = [
       dtype="bf16", seed=708),
     P("g_f16_k4", 1, 24, 24, (18, 22), 4, stride=2, pad=1, groups=3, dtype="f16", seed=709),
     P("g_ragged_h", 3, 6, 6, (37, 33), 3, stride=2, pad=1, output_padding=1, seed=710),
+    # fp32 with input widths a multiple of 4: input rows staged by TMA boxes
+    P("g_tma_cig5_cog7", 2, 15, 21, (20, 72), 3, stride=2, pad=1, output_padding=1, groups=3,
+      seed=711, bias=False),
+    P("g_tma_k4s2", 1, 8, 8, (20, 32), 4, stride=2, pad=1, seed=712),
+    P("g_tma_s13", 1, 12, 12, (17, 12), 3, stride=(1, 3), pad_lo=(0, 2), pad_hi=(1, 1),
+      dilation=(1, 2), output_padding=(0, 2), groups=2, seed=713),
+    P("g_tma_3d", 1, 16, 16, (3, 12, 12), 3, stride=(1, 2, 2), pad=1, output_padding=(0, 1, 1),
+      groups=2, seed=714),
+    P("g_tma_wide_s1", 1, 7, 8, (30, 132), 3, stride=1, pad=1, seed=715),
+    P("g_tma_ragged", 3, 6, 6, (37, 36), 3, stride=2, pad=1, output_padding=1, seed=716),
 ]
 
 

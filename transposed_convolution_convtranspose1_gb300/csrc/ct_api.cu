@@ -680,11 +680,12 @@ int ct_host_buffers_release(void) {
 }  // extern "C"
 
 extern "C" int ct_device_status(int clear, unsigned int* code) {
-    unsigned int a = 0, b = 0;
+    unsigned int a = 0, b = 0, c = 0;
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = ct::tc_error_word(&a, clear != 0);
     if (e == cudaSuccess) e = ct::tc32_error_word(&b, clear != 0);
-    if (code) *code = a | b;
+    if (e == cudaSuccess) e = ct::grouped_tma_error_word(&c, clear != 0);
+    if (code) *code = a | b | c;
     if (e != cudaSuccess) return ct::report_error(CT_ERR_CUDA, "%s", cudaGetErrorString(e));
-    return (a | b) ? CT_ERR_DEVICE_TIMEOUT : CT_OK;
+    return (a | b | c) ? CT_ERR_DEVICE_TIMEOUT : CT_OK;
 }

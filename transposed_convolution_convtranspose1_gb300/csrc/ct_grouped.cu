@@ -475,6 +475,13 @@ cudaError_t launch_grouped(const Problem& p, const void* x, const void* w, const
                            void* y, cudaStream_t stream, Profile* prof) {
     GroupedPlan pl;
     if (!make_plan(p, &pl)) return cudaErrorInvalidValue;
+    if (grouped_tma_supports(p, x)) {
+        prof_begin(prof, stream);
+        cudaError_t e = launch_grouped_tma(p, x, w, bias, y, stream);
+        prof_end(prof, stream);
+        prof_count(prof);
+        return e;
+    }
     GroupedParams P;
     std::memset(&P, 0, sizeof(P));
     P.x = x;

@@ -6,6 +6,14 @@
 
 namespace ct {
 
+// fp32 grouped gather with TMA-staged input rows for groups of 5..8 channels
+// on 2-D/3-D outputs (ct_grouped_tma.cu); launched by launch_grouped when it
+// applies.
+bool grouped_tma_supports(const Problem& p, const void* x);
+cudaError_t launch_grouped_tma(const Problem& p, const void* x, const void* w, const void* bias,
+                               void* y, cudaStream_t stream);
+cudaError_t grouped_tma_error_word(unsigned int* v, bool clear);
+
 // CUDA-core grouped/depthwise stride-phase gather (ct_grouped.cu).
 bool grouped_supports(const Problem& p);
 bool grouped_preferred(const Problem& p);
