@@ -101,9 +101,11 @@ __global__ void __launch_bounds__(kGW * 32, 4) grouped_tma_kernel(const __grid_c
     const int qh0 = hb * kGQB, q0 = qc * kGQ;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // shared memory: x tiles [jd][ic][row][col], then weights [tap][ic][oc] as {w, w}
-    float* xs = sm;
-    float2* w2 = reinterpret_cast<float2*>(sm + (size_t)P.nd_max * (kGTile / sizeof(float)));
+    // shared memory: weights [tap][ic][oc] as {w, w} at the aligned base (so
+    // that a float4 of them is one 16-byte load), then the x tiles
+    // [jd][ic][row][col] at a multiple of 512 bytes
+    float2* w2 = reinterpret_cast<float2*>(sm);
+    float* xs = sm + (size_t)P.taps * kGC * kGC * 2;
     const uint32_t bar = smem_u32(&bar_storage);
     const int x_org = (q0 + P.wmin) & ~3;         // column origin, a multiple of 4
     const int sh = q0 + P.wmin - x_org;           // 0..3
@@ -213,8 +215,8 @@ __global__ void __launch_bounds__(kGW * 32, 4) grouped_tma_kernel(const __grid_c
                     const int tdh = (P.tap[0][rd][jd] * P.K[1] + P.tap[1][rh][jh]) * P.K[2];
                     for (int jw = 0; jw < nw_; ++jw) {
                         const float* xp = xr + P.off[2][r][jw];
-                        const float4* wp =
-                            reinterpret_cast<const float4*>(w2 + (tdh + P.tap[2][r][jw]) * kGC * kGC);
+                        const float4* wp = reinterpret_cast<const float4*>(sm) +
+                                           (tdh + P.tap[2][r][jw]) * (kGC * kGC / 2);
 #pragma unroll
                         for (int ic = 0; ic < kGC; ++ic) {
                             float2 xv[kGR];
