@@ -100,15 +100,18 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-# Dominant kernel of each route: its name, the bound that applies to it and
-# the source file its DRAM traffic figure depends on.
-ROUTE_KERNEL = {
-    "gather": ("gather_kernel", "alu", "ct_gather.cu"),
-    "grouped": ("grouped_staged_kernel", "hbm", "ct_grouped.cu"),
-    "simt_gemm": ("simt_phase_gemm", "alu", "ct_simt.cu"),
-    "tc_gemm": ("tc_phase_gemm", "tensor", "ct_tc.cu"),
-    "tc32_gemm": ("tc32_phase_gemm", "tensor", "ct_tc32.cu"),
-    "bias_fill": ("bias_fill_kernel", "hbm", "ct_gather.cu"),
+# Each dominant kernel (named by the library's ct_conv_transpose_kernel): the
+# bound that applies to it and the source file its DRAM traffic figure
+# depends on.
+KERNEL_INFO = {
+    "gather_kernel": ("alu", "ct_gather.cu"),
+    "grouped_tma_kernel": ("hbm", "ct_grouped_tma.cu"),
+    "grouped_staged_kernel": ("hbm", "ct_grouped.cu"),
+    "grouped_kernel": ("hbm", "ct_grouped.cu"),
+    "simt_phase_gemm": ("alu", "ct_simt.cu"),
+    "tc_phase_gemm": ("tensor", "ct_tc.cu"),
+    "tc32_phase_gemm": ("tensor", "ct_tc32.cu"),
+    "bias_fill_kernel": ("hbm", "ct_gather.cu"),
 }
 
 
@@ -140,8 +143,17 @@ def traffic_for(kernel, src, workload):
     return e.get("dram_bytes_per_launch")
 
 
+def dominant_kernel(p):
+    """The kernel the library runs for p's main work (ct_conv_transpose_kernel)."""
+    import transposed_convolution_convtranspose1_gb300 as ct
+    return ct.ct_conv_transpose_kernel(p.B, p.C_in, p.C_out, p.spatial, p.k, p.stride, p.pad_lo,
+                                       p.pad_hi, p.dilation, p.output_padding, p.groups,
+                                       ct.dtype_code(p.torch_dtype))
+
+
 def roofline(route_name, p, main_ms, peaks, timed_alone):
-    kernel, bound, src = ROUTE_KERNEL.get(route_name, ("?", "hbm", "ct_gather.cu"))
+    kernel = dominant_kernel(p)
+    bound, src = KERNEL_INFO.get(kernel, ("hbm", "ct_gather.cu"))
     if route_name in ("gather", "simt_gemm") and p.dtype != "f32":
         bound = "alu"
     flops = 2.0 * valid_macs(p)

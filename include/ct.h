@@ -147,6 +147,23 @@ int ct_conv_transpose_route(int nd, int64_t B, int64_t C_in, int64_t C_out,
                             int* route);
 
 /*
+ * Name of the kernel that takes most of the device time of
+ * ct_conv_transpose_nd on this problem (for example "tc_phase_gemm" or
+ * "grouped_tma_kernel"; "" when the call launches nothing), written to
+ * *name as a pointer to a static string.  Host only; like the route it
+ * depends on the current device, and it assumes x is 16-byte aligned, as
+ * device allocations are (an x that is not aligned can move a grouped fp32
+ * problem from grouped_tma_kernel to grouped_staged_kernel).  Used to tie a
+ * measured time to the kernel's roofline and profile.
+ */
+int ct_conv_transpose_kernel(int nd, int64_t B, int64_t C_in, int64_t C_out,
+                             const int64_t* in_spatial, const int64_t* k,
+                             const int* stride, const int* pad_lo,
+                             const int* pad_hi, const int* dilation,
+                             const int* output_padding, int groups, int dtype,
+                             const char** name);
+
+/*
  * Forward transposed convolution on the device.
  *
  *   x, w, bias, y : device pointers owned by the caller, layouts above; bias

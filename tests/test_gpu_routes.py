@@ -87,3 +87,25 @@ def test_auto_routes_of_the_workloads():
                                          p.pad_lo, p.pad_hi, p.dilation, p.output_padding,
                                          p.groups, ct.dtype_code(p.torch_dtype))
         assert got == r, (p.name, got, r)
+
+
+def test_dominant_kernel_of_the_workloads():
+    """ct_conv_transpose_kernel names the kernel each workload's time goes
+    to: the small 2-D case (4 input channels per group) takes the staged
+    grouped kernel, the grouped workload (8 per group, fp32, width 56) the
+    TMA one; a bf16 grouped problem stays on the staged kernel."""
+    want = {0: "grouped_staged_kernel", 1: "tc32_phase_gemm", 2: "tc_phase_gemm",
+            3: "grouped_tma_kernel", 4: "tc_phase_gemm"}
+    for i, name in want.items():
+        p = synth.workload(i)
+        got = ct.ct_conv_transpose_kernel(p.B, p.C_in, p.C_out, p.spatial, p.k, p.stride,
+                                          p.pad_lo, p.pad_hi, p.dilation, p.output_padding,
+                                          p.groups, ct.dtype_code(p.torch_dtype))
+        assert got == name, (p.name, got, name)
+    p = synth.workload(3).replace(dtype="bf16")
+    got = ct.ct_conv_transpose_kernel(p.B, p.C_in, p.C_out, p.spatial, p.k, p.stride, p.pad_lo,
+                                      p.pad_hi, p.dilation, p.output_padding, p.groups,
+                                      ct.dtype_code(p.torch_dtype))
+    assert got == "grouped_staged_kernel"
+    empty = ct.ct_conv_transpose_kernel(0, 4, 6, (5,), (3,), (2,))
+    assert empty == ""

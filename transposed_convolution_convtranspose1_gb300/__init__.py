@@ -11,7 +11,8 @@ from .ct import (  # noqa: F401
     CT_ROUTE_TC32_GEMM, EXPORTS,
     ROUTE_NAMES, CtError, conv_transpose, ct_conv_transpose_nd, ct_conv_transpose_nd_host, ct_conv_transpose_nd_profiled,
     ct_conv_transpose_nd_noalloc, CT_NOALLOC_SCRATCH_BYTES,
-    ct_conv_transpose_out_shape, ct_conv_transpose_route, ct_conv_transpose_workspace_bytes,
+    ct_conv_transpose_out_shape, ct_conv_transpose_route, ct_conv_transpose_kernel,
+    ct_conv_transpose_workspace_bytes,
     ct_device_status, ct_host_buffers_release, ct_last_error, ct_status_string, ct_version,
     dtype_code, lib, ct_conv_transpose_backward_nd, ct_conv_transpose_backward_workspace_bytes,
     conv_transpose_backward, ConvTransposeFunction, conv_transpose_autograd,

@@ -358,6 +358,27 @@ int ct_conv_transpose_route(int nd, int64_t B, int64_t C_in, int64_t C_out,
     return CT_OK;
 }
 
+int ct_conv_transpose_kernel(int nd, int64_t B, int64_t C_in, int64_t C_out,
+                             const int64_t* in_spatial, const int64_t* k, const int* stride,
+                             const int* pad_lo, const int* pad_hi, const int* dilation,
+                             const int* output_padding, int groups, int dtype, const char** name) {
+    Problem p;
+    int rc = validate(&p, nd, B, C_in, C_out, in_spatial, k, stride, pad_lo, pad_hi, dilation,
+                      output_padding, groups, dtype);
+    if (rc != CT_OK) return rc;
+    if (!name) return fail(CT_ERR_NULL, "name is NULL");
+    switch (choose_route(p)) {
+        case CT_ROUTE_TC_GEMM: *name = "tc_phase_gemm"; break;
+        case CT_ROUTE_TC32_GEMM: *name = "tc32_phase_gemm"; break;
+        case CT_ROUTE_SIMT_GEMM: *name = "simt_phase_gemm"; break;
+        case CT_ROUTE_GROUPED: *name = grouped_kernel_name(p); break;
+        case CT_ROUTE_GATHER: *name = "gather_kernel"; break;
+        case CT_ROUTE_BIAS_FILL: *name = "bias_fill_kernel"; break;
+        default: *name = ""; break;
+    }
+    return CT_OK;
+}
+
 int ct_conv_transpose_route_workspace_bytes(int nd, int64_t B, int64_t C_in, int64_t C_out,
                                             const int64_t* in_spatial, const int64_t* k,
                                             const int* stride, const int* pad_lo,

@@ -471,6 +471,14 @@ bool grouped_supports(const Problem& p) {
 
 bool grouped_preferred(const Problem& p) { return p.Cog <= 16; }
 
+const char* grouped_kernel_name(const Problem& p) {
+    GroupedPlan pl;
+    if (!make_plan(p, &pl)) return "";
+    alignas(16) static const char aligned = 0;
+    if (grouped_tma_supports(p, &aligned)) return "grouped_tma_kernel";
+    return pl.staged ? "grouped_staged_kernel" : "grouped_kernel";
+}
+
 cudaError_t launch_grouped(const Problem& p, const void* x, const void* w, const void* bias,
                            void* y, cudaStream_t stream, Profile* prof) {
     GroupedPlan pl;

@@ -16,6 +16,8 @@ cudaError_t grouped_tma_error_word(unsigned int* v, bool clear);
 
 // CUDA-core grouped/depthwise stride-phase gather (ct_grouped.cu).
 bool grouped_supports(const Problem& p);
+// The kernel launch_grouped runs for p (x assumed 16-byte aligned).
+const char* grouped_kernel_name(const Problem& p);
 bool grouped_preferred(const Problem& p);
 cudaError_t launch_grouped(const Problem& p, const void* x, const void* w, const void* bias,
                            void* y, cudaStream_t stream, Profile* prof);

@@ -46,6 +46,7 @@ _vp = ctypes.c_void_p
 EXPORTS = ("ct_version", "ct_last_error", "ct_status_string",
            "ct_conv_transpose_out_shape", "ct_conv_transpose_workspace_bytes",
            "ct_conv_transpose_route", "ct_conv_transpose_route_workspace_bytes",
+           "ct_conv_transpose_kernel",
            "ct_conv_transpose_nd", "ct_conv_transpose_nd_route",
            "ct_conv_transpose_nd_host", "ct_conv_transpose_nd_profiled",
            "ct_conv_transpose_nd_noalloc", "ct_device_status", "ct_host_buffers_release",
@@ -101,6 +102,8 @@ def _declare(h):
         ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
     h.ct_conv_transpose_route.restype = ctypes.c_int
     h.ct_conv_transpose_route.argtypes = _SHAPE_ARGS + [_i32p]
+    h.ct_conv_transpose_kernel.restype = ctypes.c_int
+    h.ct_conv_transpose_kernel.argtypes = _SHAPE_ARGS + [ctypes.POINTER(ctypes.c_char_p)]
     h.ct_conv_transpose_nd.restype = ctypes.c_int
     h.ct_conv_transpose_nd.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_size_t] + _SHAPE_ARGS + [_vp]
     h.ct_conv_transpose_nd_route.restype = ctypes.c_int
@@ -233,6 +236,16 @@ def ct_conv_transpose_route(B, C_in, C_out, in_spatial, k, stride=None, pad_lo=N
     _check(lib().ct_conv_transpose_route(*_shape_args(B, C_in, C_out, ax, groups, dtype),
                                          ctypes.byref(r)))
     return int(r.value)
+
+
+def ct_conv_transpose_kernel(B, C_in, C_out, in_spatial, k, stride=None, pad_lo=None, pad_hi=None,
+                             dilation=None, output_padding=None, groups=1, dtype=CT_F32) -> str:
+    """Name of the kernel that dominates ct_conv_transpose_nd's device time here."""
+    ax = _Axes(len(in_spatial), in_spatial, k, stride, pad_lo, pad_hi, dilation, output_padding)
+    name = ctypes.c_char_p()
+    _check(lib().ct_conv_transpose_kernel(*_shape_args(B, C_in, C_out, ax, groups, dtype),
+                                          ctypes.byref(name)))
+    return name.value.decode() if name.value is not None else ""
 
 
 def _ptr(t: Optional[torch.Tensor]):
