@@ -198,3 +198,27 @@ def test_extended_call_validates_its_options_before_launch(lib):
     n = ctb.ct_conv_transpose_ex_workspace_bytes(1, 4, 6, [3], [2], [1], [0], [0], [1], [0],
                                                  1, ctb.CT_F32, ctb.CT_W_TORCH, 1)
     assert n >= 4 * 6 * 2 * 4
+
+
+def test_kernel_query_validates_before_any_device_work(lib):
+    """ct_conv_transpose_kernel rejects what ct_conv_transpose_nd rejects (a
+    bad output size, output_padding at the stride, groups not dividing C_in,
+    an integer dtype) and a NULL result pointer, all on the host."""
+    import ctypes
+    q = ctb.ct_conv_transpose_kernel
+    with pytest.raises(ctb.CtError) as e:
+        q(1, 4, 6, (1,), (1,), (1,), (1,), (1,))          # output size 1 - 2 < 1
+    assert e.value.status == ctb.CT_ERR_SHAPE
+    with pytest.raises(ctb.CtError) as e:
+        q(1, 4, 6, (5,), (3,), (2,), output_padding=(2,))
+    assert e.value.status == ctb.CT_ERR_PARAM
+    with pytest.raises(ctb.CtError) as e:
+        q(1, 6, 6, (5,), (3,), (2,), groups=4)
+    assert e.value.status == ctb.CT_ERR_GROUPS
+    with pytest.raises(ctb.CtError) as e:
+        q(1, 4, 6, (5,), (3,), (2,), dtype=7)
+    assert e.value.status == ctb.CT_ERR_DTYPE
+    ax = ctb._Axes(1, (5,), (3,), (2,), None, None, None, None)
+    rc = lib.ct_conv_transpose_kernel(*ctb._shape_args(1, 4, 6, ax, 1, ctb.CT_F32),
+                                      ctypes.cast(None, ctypes.POINTER(ctypes.c_char_p)))
+    assert rc == ctb.CT_ERR_NULL
