@@ -474,6 +474,7 @@ bool grouped_preferred(const Problem& p) { return p.Cog <= 16; }
 const char* grouped_kernel_name(const Problem& p) {
     GroupedPlan pl;
     if (!make_plan(p, &pl)) return "";
+    // asked for an input at a 16-byte aligned address, as device allocations are
     alignas(16) static const char aligned = 0;
     if (grouped_tma_supports(p, &aligned)) return "grouped_tma_kernel";
     return pl.staged ? "grouped_staged_kernel" : "grouped_kernel";
