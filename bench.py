@@ -352,6 +352,14 @@ def time_steps(r: Runner, K, flush):
     return step_ms, main_ms, launches
 
 
+def max_over_ranks(values, device):
+    """Each value's maximum over the ranks of the initialised process group:
+    the slowest rank sets every time the job reports."""
+    t = torch.tensor(values, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
 def run_ours(args):
     import transposed_convolution_convtranspose1_gb300 as ct
     from transposed_convolution_convtranspose1_gb300 import _build
@@ -406,9 +414,7 @@ def run_ours(args):
     ms = statistics.mean(step_ms)
     main = statistics.mean(main_ms)
     if world > 1:
-        t = torch.tensor([ms, main], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, main = float(t[0]), float(t[1])
+        ms, main = max_over_ranks([ms, main], dev)
 
     flops = 2.0 * valid_macs(p)
     nbytes = alg_bytes(p)
@@ -424,9 +430,7 @@ def run_ours(args):
         r.host_step()
     e2e_s = (time.perf_counter() - t0) / Ke
     if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t[0])
+        (e2e_s,) = max_over_ranks([e2e_s], dev)
     h2d, d2h = r.h2d_d2h_bytes()
 
     rl = roofline(route_name, p, main, peaks, timed_alone=True)
