@@ -411,14 +411,36 @@ int ct_conv_transpose_nd_noalloc(const void* x, const void* w, const void* bias,
                                  int groups, int dtype, void* stream);
 
 /*
- * Device-side error word written by bounded waits in the tensor-core kernels
- * (0 = none; otherwise the bits say which wait gave up: 1 producer, 2 MMA
- * issuer, 4 epilogue, 8 drain after a failure; the words of the bf16/fp16
- * and the fp32 tensor-core kernels are OR-ed).  Synchronises the current
- * device, writes the word to *code and clears it when `clear` is nonzero.
- * Returns CT_ERR_DEVICE_TIMEOUT when the word was set, CT_OK otherwise.
+ * Device-side error word written by bounded waits in the kernels that wait on
+ * asynchronous copies or MMAs (0 = none; otherwise the bits say which wait
+ * gave up: 1 TMA producer, 2 MMA issuer, 4 epilogue (tensor-core routes),
+ * 8 a drain after a give-up that itself ran out, 16 the grouped TMA kernel's
+ * copy, 32 a grouped warp pair's input copy, 64 a grouped warp pair's results;
+ * the words of every kernel file are
+ * OR-ed).  Synchronises the current device, writes the word to *code and
+ * clears it when `clear` is nonzero.  Returns CT_ERR_DEVICE_TIMEOUT when the
+ * word was set, CT_OK otherwise.  The SKaiNET pull request's rule that bad
+ * states fail loudly instead of giving silent results, applied to the device:
+ * a kernel whose wait gives up stops its work, lets every copy and MMA it has
+ * already issued finish (bounded by a fixed 2 s), frees its tensor memory,
+ * returns, and leaves its outputs unspecified; the word tells the caller.
  */
 int ct_device_status(int clear, unsigned int* code);
+
+/* Default limit of each bounded device-side wait, in nanoseconds (2 s). */
+#define CT_WAIT_LIMIT_DEFAULT_NS 2000000000ull
+
+/*
+ * Sets the limit, in nanoseconds, of every bounded device-side wait in the
+ * launches that follow (process-wide, all devices) and returns the previous
+ * limit.  The default, CT_WAIT_LIMIT_DEFAULT_NS, is far above any wait of a
+ * healthy call.  A limit of 0 makes a wait give up at the first probe that
+ * finds its copy or MMA incomplete, as if it would never arrive: tests use it
+ * to drive the give-up path of ct_device_status on purpose.  Host only; for
+ * tests and diagnostics -- calls made while the limit is small may stop early
+ * and leave y unspecified (ct_device_status then reports it).
+ */
+unsigned long long ct_set_wait_limit_ns(unsigned long long ns);
 
 #ifdef __cplusplus
 }

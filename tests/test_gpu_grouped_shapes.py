@@ -7,9 +7,15 @@ The problems cover: the grouped workload's geometry (one live W residue:
 (direct kernel), ragged bands along H, mixed strides with dilation and
 asymmetric pads, a 3-D output with a D stride, no bias, 16-bit dtypes, and
 an output that is only 4-byte aligned (2-wide stores off).  The fp32 problems
-whose input width is a multiple of 4 take the kernel whose input rows arrive
-by TMA boxes (channel boxes past the last channel, rows and columns outside
-the input read as zero).
+whose input width is a multiple of 4 take one of the two kernels whose input
+rows arrive by TMA boxes (channel boxes past the last channel, rows and
+columns outside the input read as zero): the warp-pair kernel where four
+pairs' buffers fit in shared memory, the TMA block kernel otherwise (3-D
+problems with three or four D taps); each problem names the kernel it must
+take.
+The warp-pair problems add several W chunks per row, ragged bands of 3
+rows, output depths no tap reaches, an H offset span of 3, a fused activation
+and more items than warps.
 """
 import numpy as np
 import pytest
@@ -65,10 +71,35 @@ SHAPES = [
       groups=2, seed=714),
     P("g_tma_wide_s1", 1, 7, 8, (30, 132), 3, stride=1, pad=1, seed=715),
     P("g_tma_ragged", 3, 6, 6, (37, 36), 3, stride=2, pad=1, output_padding=1, seed=716),
+    # warp-pipeline kernel: D stride 2 with a D residue no tap reaches, H span 3
+    P("g_warp_3d_dead_d", 2, 16, 16, (3, 10, 16), (1, 3, 3), stride=2, pad=(0, 1, 1),
+      output_padding=(1, 1, 1), groups=2, seed=717),
+    P("g_warp_span3", 1, 8, 8, (14, 24), (4, 3), stride=(1, 2), pad_lo=(3, 1), pad_hi=(0, 1),
+      dilation=(1, 2), output_padding=(0, 1), seed=718),
+    P("g_warp_many_items", 8, 128, 128, (40, 44), 3, stride=2, pad=1, dilation=2,
+      output_padding=1, groups=16, seed=719),
+    # four D taps: too much shared memory for the warp pairs: the TMA block kernel
+    P("g_tma_3d_k4", 1, 16, 16, (5, 12, 12), (4, 3, 3), stride=(1, 2, 2), pad=1,
+      output_padding=(0, 1, 1), groups=2, seed=720),
 ]
+
+# the kernel each fp32 TMA-eligible problem must take
+KERNEL = {"g_workload_geom": "grouped_warp_kernel", "g_tma_cig5_cog7": "grouped_warp_kernel",
+          "g_tma_k4s2": "grouped_warp_kernel", "g_tma_s13": "grouped_warp_kernel",
+          "g_tma_3d": "grouped_tma_kernel", "g_tma_3d_k4": "grouped_tma_kernel", "g_tma_wide_s1": "grouped_warp_kernel",
+          "g_tma_ragged": "grouped_warp_kernel", "g_warp_3d_dead_d": "grouped_warp_kernel",
+          "g_warp_span3": "grouped_warp_kernel", "g_warp_many_items": "grouped_warp_kernel"}
+
+
+def _kernel(p):
+    return ct.ct_conv_transpose_kernel(p.B, p.C_in, p.C_out, p.spatial, p.k, p.stride, p.pad_lo,
+                                       p.pad_hi, p.dilation, p.output_padding, p.groups,
+                                       ct.dtype_code(p.torch_dtype))
 
 
 def _check(p, pad_elems=64):
+    if p.name in KERNEL:
+        assert _kernel(p) == KERNEL[p.name], (p.name, _kernel(p))
     x, w, b = synth.make_inputs(p)
     O = ct.ct_conv_transpose_out_shape(p.spatial, p.k, p.stride, p.pad_lo, p.pad_hi, p.dilation,
                                        p.output_padding)
@@ -114,3 +145,24 @@ def test_grouped_route_is_deterministic():
         outs.append(y)
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("act", ["relu", "gelu", "sigmoid"])
+def test_grouped_warp_kernel_fuses_the_activation(act):
+    """The warp-pair kernel applies the activation in its epilogue (to
+    computed outputs and to the bias-only ones): y = act(convT(x) + b)."""
+    p = SHAPES[0]
+    assert _kernel(p) == "grouped_warp_kernel"
+    x, w, b = synth.make_inputs(p)
+    O = ct.ct_conv_transpose_out_shape(p.spatial, p.k, p.stride, p.pad_lo, p.pad_hi, p.dilation,
+                                       p.output_padding)
+    y = torch.full((p.B, p.C_out) + tuple(O), float("nan"), device="cuda")
+    ct.ct_conv_transpose_nd_ex(x.cuda(), w.cuda(), b.cuda(), y, None, p.stride, p.pad_lo,
+                               p.pad_hi, p.dilation, p.output_padding, p.groups,
+                               activation=act)
+    torch.cuda.synchronize()
+    ref = oracle.activation(oracle.conv_transpose(x, w, b, **p.attrs()), act)
+    got = y.double().cpu().numpy()
+    err = float(np.max(np.abs(got - ref)))
+    scale = max(float(np.max(np.abs(ref))), 1e-30)
+    assert err <= TOL[p.dtype] * scale, f"{act}: {err:.3e} > {TOL[p.dtype]} * {scale:.3e}"

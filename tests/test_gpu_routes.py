@@ -93,9 +93,9 @@ def test_dominant_kernel_of_the_workloads():
     """ct_conv_transpose_kernel names the kernel each workload's time goes
     to: the small 2-D case (4 input channels per group) takes the staged
     grouped kernel, the grouped workload (8 per group, fp32, width 56) the
-    TMA one; a bf16 grouped problem stays on the staged kernel."""
+    warp-pipeline one; a bf16 grouped problem stays on the staged kernel."""
     want = {0: "grouped_staged_kernel", 1: "tc32_phase_gemm", 2: "tc_phase_gemm",
-            3: "grouped_tma_kernel", 4: "tc_phase_gemm"}
+            3: "grouped_warp_kernel", 4: "tc_phase_gemm"}
     for i, name in want.items():
         p = synth.workload(i)
         got = ct.ct_conv_transpose_kernel(p.B, p.C_in, p.C_out, p.spatial, p.k, p.stride,

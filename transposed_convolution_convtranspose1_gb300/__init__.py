@@ -18,4 +18,5 @@ from .ct import (  # noqa: F401
     conv_transpose_backward, ConvTransposeFunction, conv_transpose_autograd,
     ct_conv_transpose_nd_ex, ct_conv_transpose_ex_workspace_bytes, ACTIVATIONS, CT_ACT_NONE,
     CT_ACT_RELU, CT_ACT_LEAKY_RELU, CT_ACT_SILU, CT_ACT_GELU, CT_ACT_TANH, CT_ACT_SIGMOID,
-    CT_W_TORCH, CT_W_KDHW_CI_CO, CT_W_KDHW_CO_CI)
+    CT_W_TORCH, CT_W_KDHW_CI_CO, CT_W_KDHW_CO_CI, ct_set_wait_limit_ns,
+    CT_WAIT_LIMIT_DEFAULT_NS)

@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "ct_internal.h"
@@ -160,19 +161,21 @@ int run(const Problem& p, int route, const void* x, const void* w, const void* b
         }
     }
     cudaError_t e = cudaSuccess;
+    bool act_done = false;
     switch (route) {
         case CT_ROUTE_NONE: break;
         case CT_ROUTE_BIAS_FILL: e = launch_bias_fill(p, bias, y, stream, prof); break;
         case CT_ROUTE_GATHER: e = launch_gather(p, x, w, bias, y, stream, prof); break;
-        case CT_ROUTE_GROUPED: e = launch_grouped(p, x, w, bias, y, stream, prof); break;
+        case CT_ROUTE_GROUPED: e = launch_grouped(p, x, w, bias, y, stream, prof, &act_done); break;
         case CT_ROUTE_SIMT_GEMM: e = launch_simt(p, x, w, bias, y, ws, stream, prof); break;
         case CT_ROUTE_TC_GEMM: e = launch_tc(p, x, w, bias, y, ws, stream, prof); break;
         case CT_ROUTE_TC32_GEMM: e = launch_tc32(p, x, w, bias, y, ws, stream, prof); break;
         default: e = cudaErrorInvalidValue; break;
     }
-    // the CUDA-core routes apply an activation as a second pass over y (the
-    // tcgen05 routes and the bias fill fuse it into their epilogues)
-    if (e == cudaSuccess && p.act != 0 &&
+    // the CUDA-core routes without a fused activation apply it as a second
+    // pass over y (the tcgen05 routes, the bias fill and the grouped warp
+    // kernel fuse it into their epilogues)
+    if (e == cudaSuccess && p.act != 0 && !act_done &&
         (route == CT_ROUTE_GATHER || route == CT_ROUTE_GROUPED || route == CT_ROUTE_SIMT_GEMM))
         e = launch_activation(p, y, stream, prof);
     if (owned) {
@@ -274,6 +277,12 @@ void plan_axis(const Problem& p, int axis, AxisPlan* out) {
     }
 }
 
+namespace {
+std::atomic<uint64_t> g_wait_limit_ns{CT_WAIT_LIMIT_DEFAULT_NS};
+}  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
 cudaError_t device_info(DeviceInfo* out) {
     static std::mutex mu;
     static DeviceInfo cache[64];
@@ -309,6 +318,10 @@ using namespace ct;
 extern "C" {
 
 int ct_version(void) { return 100; }
+
+unsigned long long ct_set_wait_limit_ns(unsigned long long ns) {
+    return g_wait_limit_ns.exchange(ns);
+}
 
 const char* ct_last_error(void) { return g_msg; }
 
@@ -701,12 +714,14 @@ int ct_host_buffers_release(void) {
 }  // extern "C"
 
 extern "C" int ct_device_status(int clear, unsigned int* code) {
-    unsigned int a = 0, b = 0, c = 0;
+    unsigned int a = 0, b = 0, c = 0, d = 0;
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = ct::tc_error_word(&a, clear != 0);
     if (e == cudaSuccess) e = ct::tc32_error_word(&b, clear != 0);
     if (e == cudaSuccess) e = ct::grouped_tma_error_word(&c, clear != 0);
-    if (code) *code = a | b | c;
+    if (e == cudaSuccess) e = ct::grouped_warp_error_word(&d, clear != 0);
+    const unsigned int all = a | b | c | d;
+    if (code) *code = all;
     if (e != cudaSuccess) return ct::report_error(CT_ERR_CUDA, "%s", cudaGetErrorString(e));
-    return (a | b | c) ? CT_ERR_DEVICE_TIMEOUT : CT_OK;
+    return all ? CT_ERR_DEVICE_TIMEOUT : CT_OK;
 }

@@ -476,14 +476,24 @@ const char* grouped_kernel_name(const Problem& p) {
     if (!make_plan(p, &pl)) return "";
     // asked for an input at a 16-byte aligned address, as device allocations are
     alignas(16) static const char aligned = 0;
+    if (grouped_warp_supports(p, &aligned)) return "grouped_warp_kernel";
     if (grouped_tma_supports(p, &aligned)) return "grouped_tma_kernel";
     return pl.staged ? "grouped_staged_kernel" : "grouped_kernel";
 }
 
 cudaError_t launch_grouped(const Problem& p, const void* x, const void* w, const void* bias,
-                           void* y, cudaStream_t stream, Profile* prof) {
+                           void* y, cudaStream_t stream, Profile* prof, bool* act_done) {
     GroupedPlan pl;
+    *act_done = false;
     if (!make_plan(p, &pl)) return cudaErrorInvalidValue;
+    if (grouped_warp_supports(p, x)) {
+        prof_begin(prof, stream);
+        cudaError_t e = launch_grouped_warp(p, x, w, bias, y, stream);
+        prof_end(prof, stream);
+        prof_count(prof);
+        *act_done = true;
+        return e;
+    }
     if (grouped_tma_supports(p, x)) {
         prof_begin(prof, stream);
         cudaError_t e = launch_grouped_tma(p, x, w, bias, y, stream);

@@ -17,8 +17,9 @@
 //     and l + 32, so per (tap, input channel) 8 four-byte loads at fixed
 //     offsets and 4 broadcast 16-byte weight loads feed 4 rows x 8 output
 //     channels x 2 positions = 32 packed two-lane FMAs;
-//   - the wait for the copy is bounded: past 2 s it records an error in the
-//     unit's device error word, waits (bounded) for the copy and goes on.
+//   - the wait for the copy is bounded (a launch parameter, 2 s by default):
+//     past it the kernel records an error in the unit's device error word,
+//     waits (bounded) for the copy and goes on.
 #include <algorithm>
 #include <cstring>
 
@@ -62,16 +63,8 @@ struct GtParams {
     int live_w;             // that residue
     int vecb;               // bias rows: 8-byte aligned rows of even width
     int nd_max;             // most D taps of any D residue
+    uint64_t wait_ns;       // limit of the copy's wait (0: give up at the first incomplete probe)
 };
-
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1, int c2, int c3) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
-        : "memory");
-}
 
 // The k-th H residue with (live) or without (dead) taps.
 __device__ __forceinline__ int kth_residue(const GtParams& P, int k, bool live, bool d_live) {
@@ -121,7 +114,7 @@ __global__ void __launch_bounds__(kGW * 32, 4) grouped_tma_kernel(const __grid_c
             tcg::mbar_expect_tx(bar, (uint32_t)(nd_ * kGTile));
             const int ch0 = (int)(b * P.C_in) + g * P.Cig;
             for (int jd = 0; jd < nd_; ++jd)
-                tma_load_4d(smem_u32(xs + (size_t)jd * (kGTile / sizeof(float))), &P.tmap_x, bar,
+                tcg::tma_load_4d(smem_u32(xs + (size_t)jd * (kGTile / sizeof(float))), &P.tmap_x, bar,
                             x_org, qh0 + P.offmin_h, qd + P.off[0][rd][jd], ch0);
         }
     }
@@ -172,7 +165,7 @@ __global__ void __launch_bounds__(kGW * 32, 4) grouped_tma_kernel(const __grid_c
         }
     }
     __syncthreads();  // weights stored; the barrier's initialisation visible
-    if (!tcg::mbar_wait(bar, 0, kErrGroupedCopy, &abort_flag)) tcg::mbar_drain(bar, 0);
+    if (!tcg::mbar_wait(bar, 0, kErrGroupedCopy, &abort_flag, P.wait_ns)) tcg::mbar_drain(bar, 0);
 
     const int ngrp = kGQB / kGR;
     for (int it = warp; it < n_live * ngrp; it += kGW) {
@@ -360,6 +353,7 @@ cudaError_t launch_grouped_tma(const Problem& p, const void* x, const void* w, c
     P.offmin_h = pl.offmin_h;
     P.wmin = pl.wmin;
     P.nd_max = pl.nd_max;
+    P.wait_ns = wait_limit_ns();
     const bool y2 = (p.O[2] % 2) == 0 && ((uintptr_t)y % 8) == 0;
     P.vecb = y2;
     int live = -1, n_live_w = 0;

@@ -58,6 +58,11 @@ void plan_axis(const Problem& p, int axis, AxisPlan* out);
 // Records a message for ct_last_error() on this thread and returns `status`.
 int report_error(int status, const char* fmt, ...);
 
+// Limit of every bounded device-side wait in later launches (ns; process-wide,
+// set by ct_set_wait_limit_ns, 2 s by default; 0 = give up at the first
+// incomplete probe).
+uint64_t wait_limit_ns();
+
 // Device properties cached per device.
 struct DeviceInfo {
     int device;

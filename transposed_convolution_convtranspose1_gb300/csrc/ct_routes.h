@@ -14,13 +14,23 @@ cudaError_t launch_grouped_tma(const Problem& p, const void* x, const void* w, c
                                void* y, cudaStream_t stream);
 cudaError_t grouped_tma_error_word(unsigned int* v, bool clear);
 
+// fp32 grouped gather for groups of 5..8 channels on 2-D/3-D outputs in
+// which every warp of a persistent grid runs its own double-buffered TMA
+// pipeline (ct_grouped_warp.cu); launched by launch_grouped when it applies.
+// It applies Problem.act in its epilogue.
+bool grouped_warp_supports(const Problem& p, const void* x);
+cudaError_t launch_grouped_warp(const Problem& p, const void* x, const void* w, const void* bias,
+                                void* y, cudaStream_t stream);
+cudaError_t grouped_warp_error_word(unsigned int* v, bool clear);
+
 // CUDA-core grouped/depthwise stride-phase gather (ct_grouped.cu).
 bool grouped_supports(const Problem& p);
 // The kernel launch_grouped runs for p (x assumed 16-byte aligned).
 const char* grouped_kernel_name(const Problem& p);
 bool grouped_preferred(const Problem& p);
+// *act_done says whether the launched kernel applied Problem.act itself.
 cudaError_t launch_grouped(const Problem& p, const void* x, const void* w, const void* bias,
-                           void* y, cudaStream_t stream, Profile* prof);
+                           void* y, cudaStream_t stream, Profile* prof, bool* act_done);
 
 // fp32 stride-phase implicit GEMM on CUDA cores (ct_simt.cu).
 bool simt_supports(const Problem& p);

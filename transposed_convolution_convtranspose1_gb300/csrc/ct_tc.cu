@@ -100,6 +100,7 @@ struct TcParams {
     int vec_store;        // 16-byte output stores allowed (O_w % 8 == 0, y aligned)
     int tma_store;        // SW = 2: epilogue writes 32 channels x 64 outputs per tensor store
     uint32_t epi_off;     // offset of the per-warp 4 KiB staging buffers from the ring
+    uint64_t wait_ns;     // limit of each bounded wait (0: give up at the first incomplete probe)
     int act;              // epilogue activation and its parameter
     float act_alpha;
 };
@@ -278,9 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                             const int ih = tl.qh0 + P.off[1][tl.rh][jh];
                             const int iw = tl.qw0 + P.off[2][rw][jw];
                             for (int kb = 0; kb < P.n_kblk; ++kb) {
-                                ok = __all_sync(0xffffffffu,
+                                ok = issued < (uint32_t)P.stages ||  // a fresh slot is free
+                                     __all_sync(0xffffffffu,
                                                 mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1,
-                                                          kErrProducer, &abort_flag));
+                                                          kErrProducer, &abort_flag, P.wait_ns));
                                 if (!ok) break;
                                 if (lane == 0) {
                                     const uint32_t fb = smem_u32(&full_bar[stage]);
@@ -324,8 +326,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                     const int rw = phase_of<SW>(P, tl, step);
                     const int slot = SW == 1 ? (int)(work_iter & 1) : step;
                     const uint32_t use = SW == 1 ? (work_iter >> 1) : work_iter;
-                    if (!mbar_wait(smem_u32(&sempty_bar[slot]), (use & 1) ^ 1, kErrMma,
-                                   &abort_flag)) {
+                    // a slot's first use finds it free
+                    if (use > 0 && !mbar_wait(smem_u32(&sempty_bar[slot]), (use & 1) ^ 1, kErrMma,
+                                   &abort_flag, P.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -333,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                     const int nk = phase_taps<SW>(P, tl, rw) * P.n_kblk;
                     const uint32_t d = tmem_base + slot * Sh::NP;
                     for (int j = 0; j < nk; ++j) {
-                        if (!mbar_wait(smem_u32(&full_bar[stage]), phase, kErrMma, &abort_flag)) {
+                        if (!mbar_wait(smem_u32(&full_bar[stage]), phase, kErrMma, &abort_flag, P.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                 const bool has = work && phase_taps<SW>(P, Tl, rw) > 0;
                 if (work) {
                     ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sfull_bar[st]), work_iter & 1,
-                                                           kErrEpilogue, &abort_flag));
+                                                           kErrEpilogue, &abort_flag, P.wait_ns));
                     if (!ok) break;
                     tc_fence_after();
                 }
@@ -438,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                 const bool has = work && phase_taps<SW>(P, Tl, rl) > 0;
                 if (work) {
                     ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sfull_bar[slot]), use & 1,
-                                                           kErrEpilogue, &abort_flag));
+                                                           kErrEpilogue, &abort_flag, P.wait_ns));
                     if (!ok) break;
                     tc_fence_after();
                 }
@@ -751,6 +754,7 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
     std::memset(&P, 0, sizeof(P));
     P.bias = bias;
     P.act = p.act;
+    P.wait_ns = wait_limit_ns();
     P.act_alpha = p.act_alpha;
     P.y = y;
     P.C_out = (int)p.C_out;

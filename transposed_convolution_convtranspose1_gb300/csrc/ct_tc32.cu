@@ -108,6 +108,7 @@ struct Tc32Params {
     uint32_t idesc_half;    // N = kNP / 2 (half tiles)
     uint32_t tmem_cols;
     uint32_t epi_off;       // offset of the epilogue blocks from the ring
+    uint64_t wait_ns;       // limit of each bounded wait (0: give up at the first incomplete probe)
     int act;                // epilogue activation and its parameter
     float act_alpha;
 };
@@ -243,9 +244,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
                         const int ih = tl.qh0 + P.off[1][C.rh][jh];
                         const int iw = tl.qw0 + P.off[2][C.rw][jw];
                         for (int kb = 0; kb < P.n_kblk; ++kb) {
-                            ok = __all_sync(0xffffffffu,
+                            ok = issued < (uint32_t)P.stages ||  // a fresh slot is free
+                                 __all_sync(0xffffffffu,
                                             mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1,
-                                                      kErrProducer, &abort_flag));
+                                                      kErrProducer, &abort_flag, P.wait_ns));
                             if (!ok) break;
                             if (lane == 0) {
                                 const uint32_t fb = smem_u32(&full_bar[stage]);
@@ -291,8 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
                 for (int k0 = 0; k0 < nk && ok; k0 += kChunkKB) {
                     const int slot = (int)(chunk_iter & 1);
                     const uint32_t use = chunk_iter >> 1;
-                    if (!mbar_wait(smem_u32(&sempty_bar[slot]), (use & 1) ^ 1, kErrMma,
-                                   &abort_flag)) {
+                    // a slot's first use finds it free
+                    if (use > 0 && !mbar_wait(smem_u32(&sempty_bar[slot]), (use & 1) ^ 1, kErrMma,
+                                   &abort_flag, P.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -301,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
                     const uint32_t idesc = tl.half < 0 ? P.idesc : P.idesc_half;
                     const int k1 = min(nk, k0 + kChunkKB);
                     for (int j = k0; j < k1; ++j) {
-                        if (!mbar_wait(smem_u32(&full_bar[stage]), phase, kErrMma, &abort_flag)) {
+                        if (!mbar_wait(smem_u32(&full_bar[stage]), phase, kErrMma, &abort_flag, P.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -373,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
                 const int slot = (int)(chunk_iter & 1);
                 const uint32_t use = chunk_iter >> 1;
                 ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sfull_bar[slot]), use & 1,
-                                                       kErrEpilogue, &abort_flag));
+                                                       kErrEpilogue, &abort_flag, P.wait_ns));
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t col0 = tmem_base + ((uint32_t)(q * 32) << 16) + slot * kNP + h * kEpiCols;
@@ -648,6 +651,7 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
     P.stage_bytes = (uint32_t)pl.stage_bytes;
     P.tmem_cols = 2 * kNP;
     P.act = p.act;
+    P.wait_ns = wait_limit_ns();
     P.act_alpha = p.act_alpha;
     P.idesc = (1u << 4)                              // D = f32
               | (2u << 7)                            // A = tf32

@@ -22,7 +22,10 @@ static __device__ unsigned int g_device_error = 0;
 
 namespace tcg {
 
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
+// Default limit of a bounded wait (the routes take the limit as a launch
+// parameter) and the fixed limit of the waits that drain copies and MMAs
+// already issued after a give-up.
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 
 // Error codes in g_device_error (bit flags).
 constexpr unsigned kErrProducer = 1u << 0;
@@ -66,19 +69,29 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Bounded wait on an mbarrier phase.  Returns false when the wait ran past
-// kWaitNs (after recording `code` in g_device_error and raising *abort) or
-// when another role has already given up (*abort set).
+// limit_ns (after recording `code` in g_device_error and raising *abort) or
+// when another role has already given up (*abort set).  A limit of 0 makes
+// every wait that is reached give up at once, as if what it waits for would
+// never arrive: the way tests drive the give-up path on purpose (the kernels
+// skip the waits that are satisfied by construction, such as the first use
+// of each free ring slot, so that a give-up always leaves work in flight to
+// drain).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned code,
-                                          volatile int* abort) {
+                                          volatile int* abort, uint64_t limit_ns) {
+    if (limit_ns == 0) {
+        if (code) atomicOr(&g_device_error, code);
+        if (abort) *abort = 1;
+        return false;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255) == 0) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitNs) {
+            if (abort && *abort) return false;
+            if (globaltimer_ns() - t0 > limit_ns) {
                 if (code) atomicOr(&g_device_error, code);
-                *abort = 1;
+                if (abort) *abort = 1;
                 return false;
             }
         }
@@ -102,6 +115,15 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map
         "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
         "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
         : "memory");
 }
 

@@ -51,7 +51,8 @@ EXPORTS = ("ct_version", "ct_last_error", "ct_status_string",
            "ct_conv_transpose_nd_host", "ct_conv_transpose_nd_profiled",
            "ct_conv_transpose_nd_noalloc", "ct_device_status", "ct_host_buffers_release",
            "ct_conv_transpose_backward_nd", "ct_conv_transpose_backward_workspace_bytes",
-           "ct_conv_transpose_nd_ex", "ct_conv_transpose_ex_workspace_bytes")
+           "ct_conv_transpose_nd_ex", "ct_conv_transpose_ex_workspace_bytes",
+           "ct_set_wait_limit_ns")
 
 # Size of the static scratch behind ct_conv_transpose_nd_noalloc (CT_NOALLOC_SCRATCH_BYTES).
 CT_NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -117,6 +118,8 @@ def _declare(h):
     h.ct_conv_transpose_nd_host.argtypes = [_vp, _vp, _vp, _vp] + _SHAPE_ARGS + [_vp]
     h.ct_conv_transpose_nd_noalloc.restype = ctypes.c_int
     h.ct_conv_transpose_nd_noalloc.argtypes = [_vp, _vp, _vp, _vp] + _SHAPE_ARGS + [_vp]
+    h.ct_set_wait_limit_ns.restype = ctypes.c_ulonglong
+    h.ct_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     h.ct_device_status.restype = ctypes.c_int
     h.ct_device_status.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_uint)]
     h.ct_host_buffers_release.restype = ctypes.c_int
@@ -356,6 +359,16 @@ def ct_conv_transpose_nd_noalloc(x: torch.Tensor, w: torch.Tensor, bias: Optiona
 def ct_host_buffers_release() -> None:
     """Return the device memory the host-buffer entry point keeps in its pool."""
     _check(lib().ct_host_buffers_release())
+
+
+# Default limit of each bounded device-side wait (CT_WAIT_LIMIT_DEFAULT_NS).
+CT_WAIT_LIMIT_DEFAULT_NS = 2_000_000_000
+
+
+def ct_set_wait_limit_ns(ns: int) -> int:
+    """Set the limit of every bounded device-side wait in later launches
+    (process-wide; 0 = every wait gives up at once); returns the previous one."""
+    return int(lib().ct_set_wait_limit_ns(int(ns)))
 
 
 def ct_device_status(clear: bool = True):
