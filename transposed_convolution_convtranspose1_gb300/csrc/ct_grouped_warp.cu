@@ -14,25 +14,29 @@
 // warp pair of a persistent grid (one CTA of up to 8 pairs per SM), so every
 // pair runs about the same number of items and consecutive items of a pair
 // share their group.  Each pair owns two buffers in shared memory.
-//   - The memory warp copies each item's input rows into a buffer with one
-//     TMA box [8 channels][3 + H offset span rows][64 columns] per D tap
-//     (column origin rounded down to a multiple of 4, the copy's alignment
-//     rule; rows, columns, depths and channels outside x read as zero), two
-//     items ahead; writes every output row of the pair's items that no tap
-//     reaches (bias only) at the start, so that these stores stream while the
-//     compute runs; and stores each item's results once the compute warp has
-//     left them in the item's buffer, then refills that buffer.
+//   - The memory warp stages each item's weights and tap table in a buffer and
+//     copies the item's input rows into it with one TMA box
+//     [8 channels][3 + H offset span rows][64 columns] per D tap (column
+//     origin rounded down to a multiple of 4, the copy's alignment rule; rows,
+//     columns, depths and channels outside x read as zero), two items ahead.
+//     While the compute warp works on an item, it writes the item's output
+//     rows that no tap reaches (bias only); once the compute warp has left the
+//     item's sums in the buffer, it takes them into registers, refills the
+//     buffer with the next item but one, and stores the sums with the bias
+//     and activation added.
 //   - The compute warp computes, for lane l, q_w = q0 + l and q0 + l + 32 of
 //     the 3 rows for all 8 output channels: 24 accumulators, each a pair of
 //     output channels updated by one packed two-lane FMA (the input value used
 //     twice, the pair's two weights as they lie in shared memory); per (tap,
 //     input channel) 6 four-byte input loads and 2 broadcast 16-byte weight
-//     loads feed 24 packed FMAs.  The taps of a phase come from a table of
-//     (input offset, weight offset) pairs.  It writes the last phase's
-//     results, bias added, over the input it has just consumed; earlier phases
-//     of an item with several (H, W) phases go straight to y.
+//     loads feed 24 packed FMAs.  The taps come from the item's table of
+//     (input offset, weight offset) pairs.  It leaves the raw sums over the
+//     input it has just consumed.  An item is one (H, W) phase of a cell, so
+//     cells with several live phases are several items.
 //   - With a W stride of 2 and one live W residue, a live output and its
-//     bias-only neighbour form one 8-byte store.
+//     bias-only neighbour form one 8-byte store; when moreover one H residue
+//     is live and a chunk spans the row, every row of a cell is written whole
+//     with such stores.
 // Waits are bounded (the limit is a launch parameter): a warp whose wait gives
 // up records an error in this file's device word and raises its pair's abort
 // flag; the memory warp lets the copies it issued land (bounded) and both
@@ -154,23 +158,10 @@ __device__ __forceinline__ bool live(const GwParams& P, const Item& m) {
     return m.nd > 0 && m.qa < P.qext[1][m.rh];
 }
 
-// One probe that may suspend the thread for up to hint_ns until the phase
-// completes (so that a waiting warp takes no issue slots from the others).
-__device__ __forceinline__ bool try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait of one lane (as tcg::mbar_wait, with sleeping probes): false
-// when it ran past limit_ns (recording `code` and raising *abort) or the
-// pair's abort flag rose; a limit of 0 gives up at once.
+// Bounded wait of one lane (as tcg::mbar_wait, checking the pair's abort
+// flag and the clock after every probe): false when it ran past limit_ns
+// (recording `code` and raising *abort) or the flag rose; a limit of 0 gives
+// up at once.
 __device__ __forceinline__ bool wait_lane(uint32_t bar, uint32_t parity, unsigned code, volatile int* abort,
                                           uint64_t limit_ns) {
     if (limit_ns == 0) {
@@ -180,7 +171,7 @@ __device__ __forceinline__ bool wait_lane(uint32_t bar, uint32_t parity, unsigne
     }
     const uint64_t t0 = tcg::globaltimer_ns();
     for (;;) {
-        if (try_wait_sleep(bar, parity, 20000u)) return true;
+        if (tcg::mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
         if (tcg::globaltimer_ns() - t0 > limit_ns) {
             atomicOr(&g_device_error, code);
@@ -297,7 +288,6 @@ __device__ __forceinline__ void memory_warp(const GwParams& P, int64_t i0, int64
     };
     prepare_next(0);
     prepare_next(1);
-
     int bg = -1;
     float bv[kWC], bd[kWC];
     auto load_bias = [&](int g) {
@@ -310,32 +300,50 @@ __device__ __forceinline__ void memory_warp(const GwParams& P, int64_t i0, int64
         bg = g;
     };
 
-    // Dense geometry: every output row of the item's cell, a float2 (two
-    // outputs of one W residue pair) per lane step: rows that no tap reaches
-    // (bias) in one pass, the live rows (value and bias) in the other.
-    auto dense_rows = [&](const Item& c, bool live_pass, const float* res) {
-        float* yb = out_base(P, c, plane);
-        const int half = O2 >> 1, lh = P.live_h[0], lw = P.live_w[0];
-        const int64_t plane2 = plane >> 1;  // O_w even
+    // Dense geometry: every output row of the item's cell, a float2 (the two
+    // outputs of a W residue pair) per lane step, a lane owning the pairs
+    // j = lane and lane + 32.  Rows that no tap reaches (bias) in one pass; the
+    // live rows (value, bias) in the other, from values r[i][u][oc] the lane
+    // holds in registers.
+    const int half = O2 >> 1;
+    const int64_t plane2 = plane >> 1;  // O_w even
+    auto dense_dead = [&](const Item& c) {
+        float2* yb = reinterpret_cast<float2*>(out_base(P, c, plane));
         for (int i = 0; i < kWRows; ++i) {
             const int qh = c.qa + i;
             for (int rh = 0; rh < S1; ++rh) {
                 const int oh = S1 * qh + rh;
                 if (oh >= O1) break;
-                const bool row_live = c.nd > 0 && rh == lh;
-                if (row_live != live_pass) continue;
-                float2* yr = reinterpret_cast<float2*>(yb + (int64_t)oh * O2);
-                for (int j = lane; j < half; j += 32) {
+                if (c.nd > 0 && rh == P.live_h[0]) continue;
+                float2* yr = yb + (int64_t)oh * (O2 >> 1);
 #pragma unroll
-                    for (int oc = 0; oc < kWC; ++oc) {
-                        if (oc >= P.Cog) continue;
-                        float2 val = make_float2(bd[oc], bd[oc]);
-                        if (live_pass) {
-                            const float v = gw_act<ACT>(res[(i * kWC + oc) * kWBW + j] + bv[oc], P);
-                            val = lw == 0 ? make_float2(v, bd[oc]) : make_float2(bd[oc], v);
-                        }
-                        yr[oc * plane2 + j] = val;
-                    }
+                for (int u = 0; u < 2; ++u) {
+                    const int j = lane + 32 * u;
+                    if (j >= half) continue;
+#pragma unroll
+                    for (int oc = 0; oc < kWC; ++oc)
+                        if (oc < P.Cog) yr[oc * plane2 + j] = make_float2(bd[oc], bd[oc]);
+                }
+            }
+        }
+    };
+    auto dense_live = [&](const Item& c, const float (&r)[kWRows][2][kWC]) {
+        float2* yb = reinterpret_cast<float2*>(out_base(P, c, plane));
+        const int lw = P.live_w[0];
+#pragma unroll
+        for (int i = 0; i < kWRows; ++i) {
+            const int oh = S1 * (c.qa + i) + P.live_h[0];
+            if (oh >= O1) break;
+            float2* yr = yb + (int64_t)oh * (O2 >> 1);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int j = lane + 32 * u;
+                if (j >= half) continue;
+#pragma unroll
+                for (int oc = 0; oc < kWC; ++oc) {
+                    if (oc >= P.Cog) continue;
+                    const float v = gw_act<ACT>(r[i][u][oc] + bv[oc], P);
+                    yr[oc * plane2 + j] = lw == 0 ? make_float2(v, bd[oc]) : make_float2(bd[oc], v);
                 }
             }
         }
@@ -349,7 +357,7 @@ __device__ __forceinline__ void memory_warp(const GwParams& P, int64_t i0, int64
     for (int64_t it = i0; it < i1; ++it, advance(P, m)) {
         if (P.dense) {
             load_bias(m.g);
-            dense_rows(m, false, nullptr);
+            dense_dead(m);
             if (!live(P, m)) continue;
             const int x = k & 1;
             if (!wait_all(x ? bf1 : bf0, (uint32_t)(k >> 1) & 1u, kErrWarpResult, abort, P.wait_ns)) {
@@ -357,10 +365,19 @@ __device__ __forceinline__ void memory_warp(const GwParams& P, int64_t i0, int64
                     if (issued[y] > 0) tcg::mbar_drain(y ? bc1 : bc0, (issued[y] - 1) & 1u);
                 return;
             }
-            dense_rows(m, true, x ? buf1 : buf0);
+            // the results into registers, the buffer refilled at once, then the stores
+            const float* res = x ? buf1 : buf0;  // [i][oc][64]
+            float r[kWRows][2][kWC];
+#pragma unroll
+            for (int i = 0; i < kWRows; ++i)
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int oc = 0; oc < kWC; ++oc) r[i][u][oc] = res[(i * kWC + oc) * kWBW + lane + 32 * u];
             __syncwarp();
             if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             prepare_next(x);
+            dense_live(m, r);
             ++k;
             continue;
         }
