@@ -105,6 +105,7 @@ def load_peaks():
 # depends on.
 KERNEL_INFO = {
     "gather_kernel": ("alu", "ct_gather.cu"),
+    "grouped_warp_kernel": ("hbm", "ct_grouped_warp.cu"),
     "grouped_tma_kernel": ("hbm", "ct_grouped_tma.cu"),
     "grouped_staged_kernel": ("hbm", "ct_grouped.cu"),
     "grouped_kernel": ("hbm", "ct_grouped.cu"),
@@ -221,7 +222,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                 "--format=csv,noheader,nounits", "-lms", "20", "-f", self.path],
                 stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
@@ -259,19 +260,27 @@ class ClockSampler:
                 return t + (float("0." + frac) if frac else 0.0)
             except Exception:
                 return None
+        # samples whose timestamps fall inside the timed region; when the region is
+        # shorter than the sampling period and none does, the nearest ones
+        # within 0.25 s of it, said so in "window"
         inside = [r for r in rows if ts(r) is not None and self.t0 is not None
-                  and self.t0 - 0.1 <= ts(r) <= (self.t1 or 1e18) + 0.1]
-        use = inside if inside else rows
+                  and self.t0 <= ts(r) <= (self.t1 or 1e18)]
+        window = "timed region"
+        use = inside
+        if not use and self.t0 is not None:
+            use = [r for r in rows if ts(r) is not None
+                   and self.t0 - 0.25 <= ts(r) <= (self.t1 or 1e18) + 0.25]
+            window = "within 0.25 s of the timed region (none fell inside it)"
         if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
-                    "samples": 0}
+                    "samples": 0, "samples_in_timed_region": 0}
         sm = [float(r[2]) for r in use if r[2].replace(".", "").isdigit()]
         mx = [float(r[3]) for r in use if r[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for r in use for n, v in zip(names, r[6:10]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(use), "samples_in_timed_region": len(inside)}
+                "samples": len(use), "samples_in_timed_region": len(inside), "window": window}
 
 
 # --------------------------------------------------------------------------
@@ -411,8 +420,9 @@ def run_ours(args):
     clocks.mark_end()
     clk = clocks.stop()
 
-    ms = statistics.mean(step_ms)
-    main = statistics.mean(main_ms)
+    # one statistic everywhere: the median step (and dominant-kernel) time
+    ms = statistics.median(step_ms)
+    main = statistics.median(main_ms)
     if world > 1:
         ms, main = max_over_ranks([ms, main], dev)
 
@@ -458,14 +468,16 @@ def run_ours(args):
         "wall_s_timed_region": round(wall1 - wall0, 4),
     }
 
-    if not args.no_per_config and world == 1:
-        line["per_config"] = per_config(args, dev, peaks, flush, skip=p.name)
+    # the bulky objects first and per_config last, compact, so that the tail a
+    # log keeps of this one line still holds every workload's figures
     if not args.no_backward and world == 1:
         line["backward"] = backward_per_config(dev, flush, peaks)
         if rank == 0 and not args.no_cpu_baseline:
             line["backward"]["cpu_baseline"] = backward_cpu_baseline(p, min(args.cpu_seconds, 10.0))
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p, args.cpu_seconds)
+    if not args.no_per_config and world == 1:
+        line["per_config"] = per_config(args, dev, peaks, flush, skip=p.name)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -473,6 +485,8 @@ def run_ours(args):
 
 
 def per_config(args, dev, peaks, flush, skip):
+    """Every workload, 20 L2-flushed steps each, medians: call time (ms),
+    dominant-kernel time (kernel_ms) and that kernel's roofline fraction."""
     import transposed_convolution_convtranspose1_gb300 as ct
     out = {}
     for p in synth.WORKLOADS:
@@ -485,12 +499,12 @@ def per_config(args, dev, peaks, flush, skip):
         ms, main = statistics.median(step_ms), statistics.median(main_ms)
         route_name = ct.ROUTE_NAMES.get(r.route, str(r.route))
         flops = 2.0 * valid_macs(p)
+        rl = roofline(route_name, p, main, peaks, timed_alone=True)
         out[p.name] = {
-            "route": route_name, "ms": round(ms, 5), "main_kernel_ms": round(main, 5),
-            "tflops": round(flops / (ms * 1e-3) / 1e12, 3),
-            "hbm_gbs": round(alg_bytes(p) / (ms * 1e-3) / 1e9, 2),
-            "roofline": roofline(route_name, p, main, peaks, timed_alone=True),
-            "steps": K, "stat": "median"}
+            "route": route_name, "kernel": rl["kernel"], "ms": round(ms, 5),
+            "kernel_ms": round(main, 5), "tflops": round(flops / (ms * 1e-3) / 1e12, 3),
+            "bound": rl["bound"], "achieved": rl["achieved"], "unit": rl["unit"],
+            "frac": rl["frac"], "traffic": rl["traffic"]}
         del r
         torch.cuda.empty_cache()
     return out
@@ -498,11 +512,11 @@ def per_config(args, dev, peaks, flush, skip):
 
 def backward_per_config(dev, flush, peaks):
     """Each gradient of every workload timed on its own (events around a call
-    that requests only it, L2 flushed before each): dx and dw against the fp32
-    FMA peak (CUDA-core kernels; work = the forward's 2 x valid MACs each), db
-    against HBM bandwidth (dy read once)."""
+    that requests only it, L2 flushed before each), as [median ms, fraction]:
+    dx and dw against the fp32 FMA peak (CUDA-core kernels; work = the
+    forward's 2 x valid MACs each), db against HBM bandwidth (dy read once)."""
     import transposed_convolution_convtranspose1_gb300 as ct
-    out = {}
+    out = {"format": "[ms, fraction of peak]: dx, dw of the fp32 FMA peak, db of HBM"}
     for p in synth.WORKLOADS:
         x, w, _ = synth.make_inputs(p)
         x, w = x.to(dev), w.to(dev)
@@ -538,12 +552,10 @@ def backward_per_config(dev, flush, peaks):
             if name == "db":
                 nbytes = dy.numel() * dy.element_size() + p.C_out * dy.element_size()
                 ach = nbytes / (ms * 1e-3) / 1e9
-                res[name] = {"ms": round(ms, 5), "achieved": round(ach, 2), "unit": "GB/s",
-                             "bound": "hbm", "frac": round(ach / peaks["hbm_gbs"], 4)}
+                res[name] = [round(ms, 5), round(ach / peaks["hbm_gbs"], 4)]
             else:
                 ach = flops / (ms * 1e-3) / 1e12
-                res[name] = {"ms": round(ms, 5), "achieved": round(ach, 3), "unit": "TFLOP/s",
-                             "bound": "alu", "frac": round(ach / FP32_ALU_PEAK_TFLOPS, 4)}
+                res[name] = [round(ms, 5), round(ach / FP32_ALU_PEAK_TFLOPS, 4)]
         out[p.name] = res
         del x, w, dy, dx, dw, db, ws
         torch.cuda.empty_cache()
