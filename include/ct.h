@@ -395,8 +395,10 @@ int ct_host_buffers_release(void);
  * than that is rejected with CT_ERR_WORKSPACE before any device work.
  *
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture.  All calls share the one array and
+ * (cudaGetSymbolAddress, with that device current) and caches it with the
+ * unique id of the device's context; make that first call before any stream
+ * capture.  After a cudaDeviceReset the next call finds a new context id and
+ * looks the address up again (make it, too, outside a capture).  All calls share the one array and
  * it keeps whatever the last call left there; the kernels overwrite every
  * byte of scratch they read, so no call depends on its contents.  Calls that
  * may overlap on the GPU (different streams, or concurrent host threads on

@@ -174,30 +174,38 @@ def test_package_never_imports_the_oracle():
 
 
 def test_extended_call_validates_its_options_before_launch(lib):
-    """ct_conv_transpose_nd_ex: unknown layout, flag or activation ->
-    CT_ERR_PARAM; the NKI layouts with groups != 1 -> CT_ERR_GROUPS; all
-    before any device work (CPU tensors stand in for the buffers)."""
-    x = torch.zeros((1, 4, 3))
-    w_nki = torch.zeros((2, 4, 6))   # [k, C_in, C_out]
-    y = torch.zeros((1, 6, 4))
-    cases = [(dict(w_layout=3), ctb.CT_ERR_PARAM),
-             (dict(taps_flipped=2), ctb.CT_ERR_PARAM),
-             (dict(activation=7), ctb.CT_ERR_PARAM),
-             (dict(activation=-1), ctb.CT_ERR_PARAM)]
-    for kw, want in cases:
-        args = dict(w_layout=ctb.CT_W_KDHW_CI_CO, taps_flipped=0, activation=0)
-        args.update(kw)
-        with pytest.raises(ctb.CtError) as e:
-            ctb.ct_conv_transpose_nd_ex(x, w_nki, None, y, stream=0, **args)
-        assert e.value.status == want, (kw, e.value)
-    with pytest.raises(ctb.CtError) as e:   # [k, C_in, C_out] with groups 2
-        ctb.ct_conv_transpose_nd_ex(x, w_nki, None, y, groups=2, w_layout=ctb.CT_W_KDHW_CI_CO,
-                                    stream=0)
-    assert e.value.status == ctb.CT_ERR_GROUPS
+    """ct_conv_transpose_nd_ex (the C entry point): unknown layout, flag or
+    activation -> CT_ERR_PARAM; the NKI layouts with groups != 1 ->
+    CT_ERR_GROUPS; all before any device work (the buffer pointers are never
+    touched: stand-in host addresses)."""
+    import ctypes
+    buf = (ctypes.c_float * 64)()
+    ptr = ctypes.cast(buf, ctypes.c_void_p).value
+    ax = ctb._Axes(1, (3,), (2,), None, None, None, None, None)
+
+    def call(w_layout=ctb.CT_W_KDHW_CI_CO, taps_flipped=0, activation=0, groups=1):
+        return lib.ct_conv_transpose_nd_ex(
+            ptr, ptr, None, ptr, None, 0, *ctb._shape_args(1, 4, 6, ax, groups, ctb.CT_F32),
+            int(w_layout), int(taps_flipped), int(activation), 0.01, None)
+
+    for kw in (dict(w_layout=3), dict(taps_flipped=2), dict(activation=7), dict(activation=-1)):
+        assert call(**kw) == ctb.CT_ERR_PARAM, kw
+    assert call(groups=2) == ctb.CT_ERR_GROUPS   # [k, C_in, C_out] with groups 2
     # workspace of a flipped PyTorch-layout weight: at least the weight's bytes
     n = ctb.ct_conv_transpose_ex_workspace_bytes(1, 4, 6, [3], [2], [1], [0], [0], [1], [0],
                                                  1, ctb.CT_F32, ctb.CT_W_TORCH, 1)
     assert n >= 4 * 6 * 2 * 4
+
+
+def test_binding_wants_device_tensors_on_one_device(lib):
+    """The device-buffer bindings refuse host tensors (a kernel would read host
+    memory) before calling the library."""
+    x = torch.zeros((1, 2, 3))
+    w = torch.zeros((2, 2, 2))
+    y = torch.zeros((1, 2, 4))
+    with pytest.raises(ctb.CtError, match="device tensors expected") as e:
+        ctb.ct_conv_transpose_nd(x, w, None, y, stride=1)
+    assert e.value.status == ctb.CT_ERR_PARAM
 
 
 def test_kernel_query_validates_before_any_device_work(lib):

@@ -10,6 +10,10 @@ tests use, over two calls in a row on different problems (so the second
 call starts from the scratch contents the first one left).  This file is
 collected last so that a stop-at-first-failure run has run everything else.
 """
+import ctypes
+import glob
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -85,3 +89,53 @@ def test_problem_larger_than_the_scratch_is_rejected():
     assert "scratch" in str(e.value)
     torch.cuda.synchronize()
     assert bool((y == 7.0).all())
+
+
+def _cudart():
+    """The CUDA runtime as a shared library (for the memory-pool counters)."""
+    cands = ["/usr/local/cuda/lib64/libcudart.so.13", "/usr/local/cuda/lib64/libcudart.so"]
+    cands += glob.glob(os.path.join(os.path.dirname(os.path.dirname(torch.__file__)), "nvidia",
+                                    "*", "lib", "libcudart.so*"))
+    for c in cands:
+        if os.path.exists(c):
+            try:
+                return ctypes.CDLL(c)
+            except OSError:
+                pass
+    pytest.skip("no shared CUDA runtime library to read the memory-pool counters")
+
+
+CUDA_MEMPOOL_ATTR_USED_MEM_HIGH = 8  # cudaMemPoolAttrUsedMemHigh
+
+
+def test_the_call_takes_no_stream_ordered_memory():
+    """The regular entry point without a workspace takes its scratch from the
+    device's default memory pool (cudaMallocAsync); the no-allocation entry
+    point must not.  The pool's high-water mark of used memory, reset to 0
+    before each call, tells which one allocated."""
+    rt = _cudart()
+    dev = torch.cuda.current_device()
+    pool = ctypes.c_void_p()
+    assert rt.cudaDeviceGetDefaultMemPool(ctypes.byref(pool), dev) == 0
+
+    def used_high_after(call):
+        zero = ctypes.c_uint64(0)
+        assert rt.cudaMemPoolSetAttribute(pool, CUDA_MEMPOOL_ATTR_USED_MEM_HIGH, ctypes.byref(zero)) == 0
+        call()
+        torch.cuda.synchronize()
+        v = ctypes.c_uint64(0)
+        assert rt.cudaMemPoolGetAttribute(pool, CUDA_MEMPOOL_ATTR_USED_MEM_HIGH, ctypes.byref(v)) == 0
+        return v.value
+
+    p = synth.workload(2)  # a route that needs scratch
+    x, w, b = to_device(*synth.make_inputs(p))
+    O = ct.ct_conv_transpose_out_shape(p.spatial, p.k, p.stride, p.pad_lo, p.pad_hi,
+                                       p.dilation, p.output_padding)
+    y = torch.empty((p.B, p.C_out) + O, dtype=p.torch_dtype, device="cuda")
+    a = dict(stride=p.stride, pad_lo=p.pad_lo, pad_hi=p.pad_hi, dilation=p.dilation,
+             output_padding=p.output_padding, groups=p.groups)
+    ct.ct_conv_transpose_nd_noalloc(x, w, b, y, **a)  # first call: address look-up
+    torch.cuda.synchronize()
+    # the check sees an allocation when there is one
+    assert used_high_after(lambda: ct.ct_conv_transpose_nd(x, w, b, y, None, **a)) > 0
+    assert used_high_after(lambda: ct.ct_conv_transpose_nd_noalloc(x, w, b, y, **a)) == 0

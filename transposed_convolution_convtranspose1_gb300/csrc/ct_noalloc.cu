@@ -14,6 +14,9 @@
 #include <cstdio>
 #include <mutex>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "ct_internal.h"
 
 namespace ct {
@@ -23,22 +26,58 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[CT_NOALLOC_SCRA
 
 namespace {
 
+// Driver entry points naming the current context (no link-time dependency on
+// libcuda; the runtime hands them out).
+struct CtxFns {
+    PFN_cuCtxGetCurrent_v4000 current = nullptr;
+    PFN_cuCtxGetId_v12000 id = nullptr;
+};
+
+const CtxFns& ctx_fns() {
+    static std::once_flag once;
+    static CtxFns f;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            f.current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            f.id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    return f;
+}
+
 // Device address of g_noalloc_scratch for the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is looked up
-// once per device, with that device current, and cached.
+// with that device current and cached together with the unique id of the
+// device's context.  The look-up runs again whenever that id changes, so a
+// cudaDeviceReset (which destroys the context and, with it, the module that
+// holds the array) costs one more look-up instead of leaving a dead address.
 cudaError_t noalloc_scratch_address(void** out) {
     static std::mutex mu;
     static void* addr[64] = {};
+    static unsigned long long ctx_id[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    // the device's primary context current (the runtime creates it if needed)
+    e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return e;
+    const CtxFns& f = ctx_fns();
+    unsigned long long id = 0;
+    CUcontext ctx = nullptr;
+    if (!f.current || !f.id || f.current(&ctx) != CUDA_SUCCESS || !ctx || f.id(ctx, &id) != CUDA_SUCCESS)
+        return cudaErrorNotSupported;
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    if (!addr[dev] || ctx_id[dev] != id) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return e;
         addr[dev] = p;
+        ctx_id[dev] = id;
     }
     *out = addr[dev];
     return cudaSuccess;

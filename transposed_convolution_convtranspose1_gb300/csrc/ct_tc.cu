@@ -28,7 +28,8 @@
 //                    D[oc, position] += W'[oc, k] X'[position, k], M = 128
 //                    output channels, N = NP positions (256 for strides 1-2),
 //                    K = 16 per instruction, fp32 accumulators in TMEM
-//        warps 2..5  epilogue: tcgen05.ld of each W phase's accumulator
+//        warps 2..9  epilogue (two per TMEM lane quarter): tcgen05.ld of each W
+//                    phase's accumulator
 //                    (one lane per output channel), + bias in fp32, one RNE
 //                    rounding, the W phases of a position interleaved in
 //                    registers so that each lane writes runs of consecutive

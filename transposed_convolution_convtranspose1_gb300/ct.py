@@ -266,6 +266,17 @@ def _problem_from_tensors(x, w, groups):
     return nd, x.shape[0], x.shape[1], w.shape[1] * groups, tuple(x.shape[2:]), tuple(w.shape[2:])
 
 
+def _same_device(*tensors) -> torch.device:
+    """The one CUDA device all given tensors (None skipped) live on."""
+    devs = {t.device for t in tensors if t is not None}
+    if len(devs) != 1:
+        raise CtError(CT_ERR_PARAM, f"tensors must share one device, got {sorted(map(str, devs))}")
+    d = devs.pop()
+    if d.type != "cuda":
+        raise CtError(CT_ERR_PARAM, f"device tensors expected, got {d}")
+    return d
+
+
 def _stream_handle(stream, device):
     if stream is None:
         return torch.cuda.current_stream(device).cuda_stream
@@ -290,14 +301,21 @@ def ct_conv_transpose_nd(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.
         if t is not None and t.dtype != x.dtype:
             raise CtError(CT_ERR_DTYPE, "x, w, bias and y must share one dtype")
     ax = _Axes(nd, I, K, stride, pad_lo, pad_hi, dilation, output_padding)
-    s = _stream_handle(stream, x.device)
+    if dtype_code(x.dtype) == _BAD_DTYPE_CODE:
+        # an unsupported element type: the library's validation names it
+        r = ctypes.c_int(-1)
+        _check(lib().ct_conv_transpose_route(*_shape_args(B, C_in, C_out, ax, groups,
+                                                          _BAD_DTYPE_CODE), ctypes.byref(r)))
+    dev = _same_device(x, w, bias, y, workspace)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     args = [_ptr(x), _ptr(w), _ptr(bias), _ptr(y), _ptr(workspace), ws_bytes,
             *_shape_args(B, C_in, C_out, ax, groups, dtype_code(x.dtype))]
-    if route == CT_ROUTE_AUTO:
-        rc = lib().ct_conv_transpose_nd(*args, s)
-    else:
-        rc = lib().ct_conv_transpose_nd_route(*args, int(route), s)
+    with torch.cuda.device(dev):  # the library works on the current device
+        s = _stream_handle(stream, dev)
+        if route == CT_ROUTE_AUTO:
+            rc = lib().ct_conv_transpose_nd(*args, s)
+        else:
+            rc = lib().ct_conv_transpose_nd_route(*args, int(route), s)
     _check(rc)
 
 
@@ -312,15 +330,18 @@ def ct_conv_transpose_nd_profiled(x, w, bias, y, workspace=None, stride=None, pa
     """
     nd, B, C_in, C_out, I, K = _problem_from_tensors(x, w, groups)
     ax = _Axes(nd, I, K, stride, pad_lo, pad_hi, dilation, output_padding)
-    s = _stream_handle(stream, x.device)
+    dev = _same_device(x, w, bias, y, workspace)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     n = ctypes.c_int(0)
     r = ctypes.c_int(-1)
     ev = lambda e: None if e is None else e.cuda_event
-    _check(lib().ct_conv_transpose_nd_profiled(
-        _ptr(x), _ptr(w), _ptr(bias), _ptr(y), _ptr(workspace), ws_bytes,
-        *_shape_args(B, C_in, C_out, ax, groups, dtype_code(x.dtype)), int(route), s,
-        ev(main_start), ev(main_stop), ctypes.byref(n), ctypes.byref(r)))
+    with torch.cuda.device(dev):
+        s = _stream_handle(stream, dev)
+        rc = lib().ct_conv_transpose_nd_profiled(
+            _ptr(x), _ptr(w), _ptr(bias), _ptr(y), _ptr(workspace), ws_bytes,
+            *_shape_args(B, C_in, C_out, ax, groups, dtype_code(x.dtype)), int(route), s,
+            ev(main_start), ev(main_stop), ctypes.byref(n), ctypes.byref(r))
+    _check(rc)
     return int(n.value), int(r.value)
 
 
@@ -350,10 +371,13 @@ def ct_conv_transpose_nd_noalloc(x: torch.Tensor, w: torch.Tensor, bias: Optiona
     if bias is not None and tuple(bias.shape) != (C_out,):
         raise CtError(CT_ERR_BIAS, f"bias must have shape [{C_out}], got {tuple(bias.shape)}")
     ax = _Axes(nd, I, K, stride, pad_lo, pad_hi, dilation, output_padding)
-    s = _stream_handle(stream, x.device)
-    _check(lib().ct_conv_transpose_nd_noalloc(
-        _ptr(x), _ptr(w), _ptr(bias), _ptr(y),
-        *_shape_args(B, C_in, C_out, ax, groups, dtype_code(x.dtype)), s))
+    dev = _same_device(x, w, bias, y)
+    with torch.cuda.device(dev):
+        s = _stream_handle(stream, dev)
+        rc = lib().ct_conv_transpose_nd_noalloc(
+            _ptr(x), _ptr(w), _ptr(bias), _ptr(y),
+            *_shape_args(B, C_in, C_out, ax, groups, dtype_code(x.dtype)), s)
+    _check(rc)
 
 
 def ct_host_buffers_release() -> None:
@@ -426,10 +450,13 @@ def ct_conv_transpose_backward_nd(x: torch.Tensor, w: torch.Tensor, dy: torch.Te
     nd, B, C_in, C_out, I, K = _problem_from_tensors(x, w, groups)
     ax = _Axes(nd, I, K, stride, pad_lo, pad_hi, dilation, output_padding)
     nws = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    s = _stream_handle(stream, dy.device)
-    _check(lib().ct_conv_transpose_backward_nd(
-        _ptr(x), _ptr(w), _ptr(dy), _ptr(dx), _ptr(dw), _ptr(db), _ptr(workspace), nws,
-        *_shape_args(B, C_in, C_out, ax, groups, dtype_code(dy.dtype)), s))
+    dev = _same_device(x, w, dy, dx, dw, db, workspace)
+    with torch.cuda.device(dev):
+        s = _stream_handle(stream, dev)
+        rc = lib().ct_conv_transpose_backward_nd(
+            _ptr(x), _ptr(w), _ptr(dy), _ptr(dx), _ptr(dw), _ptr(db), _ptr(workspace), nws,
+            *_shape_args(B, C_in, C_out, ax, groups, dtype_code(dy.dtype)), s)
+    _check(rc)
 
 
 def conv_transpose_backward(x: torch.Tensor, w: torch.Tensor, dy: torch.Tensor, stride=1,
@@ -513,9 +540,12 @@ def ct_conv_transpose_nd_ex(x: torch.Tensor, w: torch.Tensor, bias: Optional[tor
     act = ACTIVATIONS[activation] if isinstance(activation, str) else int(activation)
     ax = _Axes(nd, I, K, stride, pad_lo, pad_hi, dilation, output_padding)
     nws = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    s = _stream_handle(stream, x.device)
-    _check(lib().ct_conv_transpose_nd_ex(
-        _ptr(x), _ptr(w), _ptr(bias), _ptr(y), _ptr(workspace), nws,
-        *_shape_args(B, C_in, C_out, ax, groups, dtype_code(x.dtype)), int(w_layout),
-        int(taps_flipped), act, float(activation_alpha), s))
+    dev = _same_device(x, w, bias, y, workspace)
+    with torch.cuda.device(dev):
+        s = _stream_handle(stream, dev)
+        rc = lib().ct_conv_transpose_nd_ex(
+            _ptr(x), _ptr(w), _ptr(bias), _ptr(y), _ptr(workspace), nws,
+            *_shape_args(B, C_in, C_out, ax, groups, dtype_code(x.dtype)), int(w_layout),
+            int(taps_flipped), act, float(activation_alpha), s)
+    _check(rc)
 
