@@ -131,17 +131,24 @@ def _src_sha(fname):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def traffic_for(kernel, src, workload):
-    """DRAM bytes per launch from the committed ncu summary, if still valid."""
+def traffic_for(kernel, workload):
+    """(DRAM bytes of the dominant kernel, whole-call traffic) from the
+    committed capture (profiles/traffic.json), while the source of every
+    kernel of the call still matches; (None, None) otherwise."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
-        return None
+        return None, None
     with open(path) as f:
         d = json.load(f)
-    e = d.get(f"{kernel}@{workload}")
-    if not e or e.get("source_sha") != _src_sha(src):
-        return None
-    return e.get("dram_bytes_per_launch")
+    e = d.get("workloads", {}).get(workload)
+    if not e or any(_src_sha(src) != h for src, h in e.get("sources", {}).items()):
+        return None, None
+    k = e["kernels"].get(kernel)
+    kernel_bytes = None if k is None else k["dram_read"] + k["dram_write"]
+    c = e["call"]
+    call = {"dram_read": c["dram_read"], "sm_write": c["sm_write"], "traffic": c["traffic"],
+            "vs_algorithmic": round(c["traffic"] / e["algorithmic_bytes"], 3)}
+    return kernel_bytes, call
 
 
 def dominant_kernel(p):
@@ -154,7 +161,7 @@ def dominant_kernel(p):
 
 def roofline(route_name, p, main_ms, peaks, timed_alone):
     kernel = dominant_kernel(p)
-    bound, src = KERNEL_INFO.get(kernel, ("hbm", "ct_gather.cu"))
+    bound, _ = KERNEL_INFO.get(kernel, ("hbm", "ct_gather.cu"))
     if route_name in ("gather", "simt_gemm") and p.dtype != "f32":
         bound = "alu"
     flops = 2.0 * valid_macs(p)
@@ -180,10 +187,10 @@ def roofline(route_name, p, main_ms, peaks, timed_alone):
         basis = "HBM copy bandwidth"
         achieved = nbytes / (main_ms * 1e-3) / 1e9
         unit = "GB/s"
+    kernel_bytes, call = traffic_for(kernel, p.name)
     return {"bound": bound, "kernel": kernel, "achieved": round(achieved, 3),
             "peak": round(peak, 3), "unit": unit, "frac": round(achieved / peak, 4),
-            "peak_basis": basis,
-            "traffic": traffic_for(kernel, src, p.name),
+            "peak_basis": basis, "traffic": kernel_bytes, "call_traffic": call,
             "algorithmic_bytes": nbytes, "algorithmic_flop": flops}
 
 
@@ -504,7 +511,8 @@ def per_config(args, dev, peaks, flush, skip):
             "route": route_name, "kernel": rl["kernel"], "ms": round(ms, 5),
             "kernel_ms": round(main, 5), "tflops": round(flops / (ms * 1e-3) / 1e12, 3),
             "bound": rl["bound"], "achieved": rl["achieved"], "unit": rl["unit"],
-            "frac": rl["frac"], "traffic": rl["traffic"]}
+            "frac": rl["frac"], "traffic": rl["traffic"],
+            "call_traffic_ratio": rl["call_traffic"]["vs_algorithmic"] if rl["call_traffic"] else None}
         del r
         torch.cuda.empty_cache()
     return out

@@ -327,7 +327,7 @@ __device__ __forceinline__ void memory_warp(const GwParams& P, int64_t i0, int64
             }
         }
     };
-    auto dense_live = [&](const Item& c, const float (&r)[kWRows][2][kWC]) {
+    auto dense_live = [&](const Item& c, const float (&r)[kWRows][2][kWC], auto act) {
         float2* yb = reinterpret_cast<float2*>(out_base(P, c, plane));
         const int lw = P.live_w[0];
 #pragma unroll
@@ -342,7 +342,7 @@ __device__ __forceinline__ void memory_warp(const GwParams& P, int64_t i0, int64
 #pragma unroll
                 for (int oc = 0; oc < kWC; ++oc) {
                     if (oc >= P.Cog) continue;
-                    const float v = gw_act<ACT>(r[i][u][oc] + bv[oc], P);
+                    const float v = act(r[i][u][oc] + bv[oc]);
                     yr[oc * plane2 + j] = lw == 0 ? make_float2(v, bd[oc]) : make_float2(bd[oc], v);
                 }
             }
@@ -365,8 +365,8 @@ __device__ __forceinline__ void memory_warp(const GwParams& P, int64_t i0, int64
                     if (issued[y] > 0) tcg::mbar_drain(y ? bc1 : bc0, (issued[y] - 1) & 1u);
                 return;
             }
-            // the results into registers, the buffer refilled at once, then the stores
             const float* res = x ? buf1 : buf0;  // [i][oc][64]
+            // the results into registers, the buffer refilled at once, then the stores
             float r[kWRows][2][kWC];
 #pragma unroll
             for (int i = 0; i < kWRows; ++i)
@@ -377,7 +377,20 @@ __device__ __forceinline__ void memory_warp(const GwParams& P, int64_t i0, int64
             __syncwarp();
             if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             prepare_next(x);
-            dense_live(m, r);
+            if constexpr (ACT) {
+                // one dispatch on the activation, then its code at every store
+                switch (P.act) {
+                    case 1: dense_live(m, r, [&](float v) { return act_fixed<1>(v, P.act_alpha); }); break;
+                    case 2: dense_live(m, r, [&](float v) { return act_fixed<2>(v, P.act_alpha); }); break;
+                    case 3: dense_live(m, r, [&](float v) { return act_fixed<3>(v, P.act_alpha); }); break;
+                    case 4: dense_live(m, r, [&](float v) { return act_fixed<4>(v, P.act_alpha); }); break;
+                    case 5: dense_live(m, r, [&](float v) { return act_fixed<5>(v, P.act_alpha); }); break;
+                    case 6: dense_live(m, r, [&](float v) { return act_fixed<6>(v, P.act_alpha); }); break;
+                    default: dense_live(m, r, [](float v) { return v; }); break;
+                }
+            } else {
+                dense_live(m, r, [](float v) { return v; });
+            }
             ++k;
             continue;
         }

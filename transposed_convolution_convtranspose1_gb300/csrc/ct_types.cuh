@@ -37,14 +37,27 @@ __device__ __forceinline__ void fma2(float2& d, const float2 a, const float2 b) 
 // Activation (ct_activation codes of include/ct.h) of an fp32 value after
 // the bias: 1 relu, 2 leaky relu (alpha), 3 silu, 4 gelu (erf form),
 // 5 tanh, 6 sigmoid; anything else leaves v unchanged.
+// act_fixed<A> is the same function for a compile-time code A (for loops that
+// dispatch once on the code and then run one function at every site).
+template <int A>
+__device__ __forceinline__ float act_fixed(float v, float alpha) {
+    if constexpr (A == 1) return v > 0.f ? v : 0.f;
+    else if constexpr (A == 2) return v >= 0.f ? v : alpha * v;
+    else if constexpr (A == 3) return v / (1.f + expf(-v));
+    else if constexpr (A == 4) return 0.5f * v * (1.f + erff(v * 0.70710678118654752f));
+    else if constexpr (A == 5) return tanhf(v);
+    else if constexpr (A == 6) return 1.f / (1.f + expf(-v));
+    else return v;
+}
+
 __device__ __forceinline__ float act_f32(float v, int act, float alpha) {
     switch (act) {
-        case 1: return v > 0.f ? v : 0.f;
-        case 2: return v >= 0.f ? v : alpha * v;
-        case 3: return v / (1.f + expf(-v));
-        case 4: return 0.5f * v * (1.f + erff(v * 0.70710678118654752f));
-        case 5: return tanhf(v);
-        case 6: return 1.f / (1.f + expf(-v));
+        case 1: return act_fixed<1>(v, alpha);
+        case 2: return act_fixed<2>(v, alpha);
+        case 3: return act_fixed<3>(v, alpha);
+        case 4: return act_fixed<4>(v, alpha);
+        case 5: return act_fixed<5>(v, alpha);
+        case 6: return act_fixed<6>(v, alpha);
         default: return v;
     }
 }
