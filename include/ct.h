@@ -417,8 +417,9 @@ int ct_conv_transpose_nd_noalloc(const void* x, const void* w, const void* bias,
  * asynchronous copies or MMAs (0 = none; otherwise the bits say which wait
  * gave up: 1 TMA producer, 2 MMA issuer, 4 epilogue (tensor-core routes),
  * 8 a drain after a give-up that itself ran out, 16 the grouped TMA kernel's
- * copy, 32 a grouped warp pair's input copy, 64 a grouped warp pair's results;
- * the words of every kernel file are
+ * copy, 32 a grouped warp pair's input copy, 64 a grouped warp pair's results,
+ * 128 a staged copy of the backward pass's small-group weight-gradient
+ * kernel; the words of every kernel file are
  * OR-ed).  Synchronises the current device, writes the word to *code and
  * clears it when `clear` is nonzero.  Returns CT_ERR_DEVICE_TIMEOUT when the
  * word was set, CT_OK otherwise.  The SKaiNET pull request's rule that bad

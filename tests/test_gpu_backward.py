@@ -102,6 +102,69 @@ def test_backward_grid_matches_oracle(p):
     _check_all(p)
 
 
+# Small channel groups (at most 8 input and 8 output channels each), the
+# shapes of the dedicated grouped dw kernel: 1-D, 2-D and 3-D, dilation, ragged
+# bands (H not a multiple of 4), 25 taps, a 1x1 kernel, and one with 36 taps
+# (beyond that kernel, so the general dw kernel takes it).
+SMALL_GROUPS = [
+    P("sg_2d_full8", 2, 64, 64, (13, 10), 3, stride=2, pad=1, dilation=2, output_padding=1,
+      groups=8, seed=3001),
+    P("sg_2d_5x7_k5", 1, 15, 21, (9, 11), 5, stride=(1, 2), pad=2, groups=3, seed=3002),
+    P("sg_3d", 2, 16, 12, (3, 6, 5), 3, stride=(2, 1, 2), pad=1, output_padding=(1, 0, 1),
+      groups=2, seed=3003),
+    P("sg_1d", 3, 12, 16, (37,), 4, stride=3, pad=1, dilation=2, groups=4, seed=3004),
+    P("sg_k1", 2, 8, 8, (7, 7), 1, stride=2, groups=2, seed=3005),
+    P("sg_36taps", 1, 8, 8, (4, 5, 6), (3, 3, 4), stride=2, pad=1, groups=2, seed=3006),
+    P("sg_bf16", 2, 32, 32, (10, 12), 4, stride=2, pad=1, groups=4, dtype="bf16", seed=3007),
+    P("sg_f16_c1", 2, 6, 6, (5, 9), 3, stride=2, groups=6, dtype="f16", seed=3008),
+    # fp32 (staged by bulk row copies): widths that are not multiples of 4,
+    # a 3-D kernel, pad_lo 6 on W, many bands
+    P("sg_tma_2d", 2, 32, 24, (13, 16), 3, stride=2, pad=1, output_padding=1, groups=4, seed=3009),
+    P("sg_tma_3d", 1, 16, 16, (3, 6, 8), 3, stride=(2, 1, 2), pad=1, output_padding=(1, 0, 1),
+      groups=2, seed=3010),
+    P("sg_tma_k5_pad6", 1, 10, 14, (9, 12), 5, stride=(1, 2), pad=(2, 6), output_padding=(0, 1),
+      groups=2, seed=3011),
+    P("sg_tma_many_bands", 3, 8, 8, (41, 8), (2, 4), stride=(1, 4), pad=(0, 0), groups=1,
+      seed=3012),
+]
+
+
+@pytest.mark.parametrize("p", SMALL_GROUPS, ids=lambda p: p.name)
+def test_backward_small_groups_match_oracle(p):
+    _check_all(p, seed=3)
+
+
+def test_grouped_dw_does_not_depend_on_pointer_alignment():
+    """The small-group dw kernel stages fp32 rows by bulk copies widened to
+    16-byte boundaries, so x and dy may start anywhere a float may: views one
+    and three floats into their buffers must give the same dw, bit for bit,
+    as 256-byte aligned tensors (the same products summed in the same order)."""
+    p = P("sg_align", 2, 32, 32, (14, 20), 3, stride=2, pad=2, dilation=2, output_padding=1,
+          groups=4, seed=3013)
+    x, w, _ = synth.make_inputs(p)
+    dy = _dy_for(p, 77)
+    xd, wd, dyd = x.cuda(), w.cuda(), dy.cuda()
+
+    def shifted(t, k):
+        buf = torch.empty(t.numel() + k, device="cuda")
+        v = buf[k:].view_as(t)
+        v.copy_(t)
+        return v
+
+    x1, dy3 = shifted(xd, 1), shifted(dyd, 3)
+    assert x1.data_ptr() % 16 != 0 and dy3.data_ptr() % 16 != 0
+    out = []
+    for xi, dyi in ((xd, dyd), (x1, dy3)):
+        dw = torch.full_like(wd, float("nan"))
+        ct.ct_conv_transpose_backward_nd(xi, wd, dyi, None, dw, None, None, p.stride, p.pad_lo,
+                                         p.pad_hi, p.dilation, p.output_padding, p.groups)
+        out.append(dw)
+    torch.cuda.synchronize()
+    assert torch.equal(out[0], out[1])
+    _, rdw, _ = oracle.conv_transpose_backward(x, w, dy, **p.attrs(), need=("dw",))
+    _check(p, out[0], rdw, "dw")
+
+
 @pytest.mark.parametrize("i", [0, 1, 3])
 def test_backward_workload_matches_oracle(i):
     _check_all(synth.workload(i))

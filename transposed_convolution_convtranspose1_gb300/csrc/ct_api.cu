@@ -714,13 +714,14 @@ int ct_host_buffers_release(void) {
 }  // extern "C"
 
 extern "C" int ct_device_status(int clear, unsigned int* code) {
-    unsigned int a = 0, b = 0, c = 0, d = 0;
+    unsigned int a = 0, b = 0, c = 0, d = 0, f = 0;
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = ct::tc_error_word(&a, clear != 0);
     if (e == cudaSuccess) e = ct::tc32_error_word(&b, clear != 0);
     if (e == cudaSuccess) e = ct::grouped_tma_error_word(&c, clear != 0);
     if (e == cudaSuccess) e = ct::grouped_warp_error_word(&d, clear != 0);
-    const unsigned int all = a | b | c | d;
+    if (e == cudaSuccess) e = ct::backward_error_word(&f, clear != 0);
+    const unsigned int all = a | b | c | d | f;
     if (code) *code = all;
     if (e != cudaSuccess) return ct::report_error(CT_ERR_CUDA, "%s", cudaGetErrorString(e));
     return all ? CT_ERR_DEVICE_TIMEOUT : CT_OK;

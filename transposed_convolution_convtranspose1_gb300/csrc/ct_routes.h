@@ -22,6 +22,8 @@ bool grouped_warp_supports(const Problem& p, const void* x);
 cudaError_t launch_grouped_warp(const Problem& p, const void* x, const void* w, const void* bias,
                                 void* y, cudaStream_t stream);
 cudaError_t grouped_warp_error_word(unsigned int* v, bool clear);
+// Error word of the backward kernels (the small-group dw kernel's staged copies).
+cudaError_t backward_error_word(unsigned int* v, bool clear);
 
 // CUDA-core grouped/depthwise stride-phase gather (ct_grouped.cu).
 bool grouped_supports(const Problem& p);
