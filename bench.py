@@ -521,10 +521,13 @@ def per_config(args, dev, peaks, flush, skip):
 def backward_per_config(dev, flush, peaks):
     """Each gradient of every workload timed on its own (events around a call
     that requests only it, L2 flushed before each), as [median ms, fraction]:
-    dx and dw against the fp32 FMA peak (CUDA-core kernels; work = the
-    forward's 2 x valid MACs each), db against HBM bandwidth (dy read once)."""
+    dx and dw against the fp32 FMA peak on the CUDA-core kernels, against the
+    measured bf16 tensor peak where the gradient runs on the tensor cores
+    (third element "t"; work = the forward's 2 x valid MACs each), db against
+    HBM bandwidth (dy read once)."""
     import transposed_convolution_convtranspose1_gb300 as ct
-    out = {"format": "[ms, fraction of peak]: dx, dw of the fp32 FMA peak, db of HBM"}
+    out = {"format": "[ms, fraction of peak]: dx, dw of the fp32 FMA peak (of the bf16 tensor peak "
+                     "when marked t: tcgen05 kernel), db of HBM"}
     for p in synth.WORKLOADS:
         x, w, _ = synth.make_inputs(p)
         x, w = x.to(dev), w.to(dev)
@@ -538,6 +541,9 @@ def backward_per_config(dev, flush, peaks):
             p.output_padding, p.groups, ct.dtype_code(p.torch_dtype))
         ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
         flops = 2.0 * valid_macs(p)
+        kern = dict(zip(("dx", "dw"), ct.ct_conv_transpose_backward_kernels(
+            p.B, p.C_in, p.C_out, p.spatial, p.k, p.stride, p.pad_lo, p.pad_hi, p.dilation,
+            p.output_padding, p.groups, ct.dtype_code(p.torch_dtype))))
         res = {}
         for name, args in (("dx", (dx, None, None)), ("dw", (None, dw, None)),
                            ("db", (None, None, db))):
@@ -561,6 +567,9 @@ def backward_per_config(dev, flush, peaks):
                 nbytes = dy.numel() * dy.element_size() + p.C_out * dy.element_size()
                 ach = nbytes / (ms * 1e-3) / 1e9
                 res[name] = [round(ms, 5), round(ach / peaks["hbm_gbs"], 4)]
+            elif kern[name] == "tc_phase_gemm":
+                ach = flops / (ms * 1e-3) / 1e12
+                res[name] = [round(ms, 5), round(ach / peaks["bf16_tflops"], 4), "t"]
             else:
                 ach = flops / (ms * 1e-3) / 1e12
                 res[name] = [round(ms, 5), round(ach / FP32_ALU_PEAK_TFLOPS, 4)]

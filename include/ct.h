@@ -356,7 +356,12 @@ int ct_conv_transpose_backward_nd(const void* x, const void* w, const void* dy,
                                   const int* output_padding, int groups,
                                   int dtype, void* stream);
 
-/* Workspace bytes of ct_conv_transpose_backward_nd (dw's per-slice partials). */
+/*
+ * Workspace bytes of ct_conv_transpose_backward_nd: the larger of dw's
+ * per-slice partials and, when dx runs on the tensor cores (bf16/fp16,
+ * groups of 1, at least 16 channels each side), dy's channels-last copy and
+ * the gathered weights.  Covers a call that requests any of dx, dw and db.
+ */
 int ct_conv_transpose_backward_workspace_bytes(int nd, int64_t B, int64_t C_in,
                                                int64_t C_out,
                                                const int64_t* in_spatial,
@@ -365,6 +370,25 @@ int ct_conv_transpose_backward_workspace_bytes(int nd, int64_t B, int64_t C_in,
                                                const int* dilation,
                                                const int* output_padding,
                                                int groups, int dtype, size_t* bytes);
+
+/*
+ * Names of the kernels that take most of the device time of the input
+ * gradient and of the weight gradient of ct_conv_transpose_backward_nd on
+ * this problem, written to *dx_kernel and *dw_kernel as pointers to static
+ * strings: "tc_phase_gemm" (dx on the tensor cores: bf16/fp16, groups of 1,
+ * at least 16 channels each side) or "bwd_dx_kernel"; "bwd_dw_grouped_kernel"
+ * (groups of at most 8 input and 8 output channels, at most 27 taps) or
+ * "bwd_dw_kernel"; "" for an empty gradient.  Host only; depends on the
+ * current device.  Errors as ct_conv_transpose_backward_workspace_bytes.
+ */
+int ct_conv_transpose_backward_kernels(int nd, int64_t B, int64_t C_in,
+                                       int64_t C_out, const int64_t* in_spatial,
+                                       const int64_t* k, const int* stride,
+                                       const int* pad_lo, const int* pad_hi,
+                                       const int* dilation,
+                                       const int* output_padding, int groups,
+                                       int dtype, const char** dx_kernel,
+                                       const char** dw_kernel);
 
 /*
  * Returns the memory the host-buffer entry point keeps in its pool on the

@@ -230,3 +230,30 @@ def test_kernel_query_validates_before_any_device_work(lib):
     rc = lib.ct_conv_transpose_kernel(*ctb._shape_args(1, 4, 6, ax, 1, ctb.CT_F32),
                                       ctypes.cast(None, ctypes.POINTER(ctypes.c_char_p)))
     assert rc == ctb.CT_ERR_NULL
+
+
+def test_backward_kernel_query_validates_on_the_host(lib):
+    """ct_conv_transpose_backward_kernels rejects a bad shape, groups that do
+    not divide the channels, an integer dtype and NULL result pointers, and
+    on a problem the backward call accepts it names one kernel per gradient
+    from the two each gradient has (the tensor-core dx needs an sm_103 device,
+    which this host check does not assume)."""
+    import ctypes
+    q = ctb.ct_conv_transpose_backward_kernels
+    with pytest.raises(ctb.CtError) as e:
+        q(1, 4, 6, (1,), (1,), (1,), (1,), (1,))
+    assert e.value.status == ctb.CT_ERR_SHAPE
+    with pytest.raises(ctb.CtError) as e:
+        q(1, 6, 6, (5,), (3,), (2,), groups=4)
+    assert e.value.status == ctb.CT_ERR_GROUPS
+    with pytest.raises(ctb.CtError) as e:
+        q(1, 4, 6, (5,), (3,), (2,), dtype=7)
+    assert e.value.status == ctb.CT_ERR_DTYPE
+    ax = ctb._Axes(1, (5,), (3,), (2,), None, None, None, None)
+    null = ctypes.cast(None, ctypes.POINTER(ctypes.c_char_p))
+    rc = lib.ct_conv_transpose_backward_kernels(*ctb._shape_args(1, 4, 6, ax, 1, ctb.CT_F32), null, null)
+    assert rc == ctb.CT_ERR_NULL
+    dx, dw = q(2, 64, 32, (9, 9), (3, 3), (2, 2), dtype=ctb.CT_BF16)
+    assert dx in ("tc_phase_gemm", "bwd_dx_kernel") and dw == "bwd_dw_kernel"
+    assert q(2, 16, 16, (9, 9), (3, 3), (2, 2), groups=2)[1] == "bwd_dw_grouped_kernel"
+    assert q(0, 16, 16, (9, 9), (3, 3), (2, 2))[0] == ""

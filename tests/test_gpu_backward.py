@@ -134,6 +134,52 @@ def test_backward_small_groups_match_oracle(p):
     _check_all(p, seed=3)
 
 
+# 16-bit types, groups of 1, at least 16 channels each side: dx on the tcgen05
+# GEMM (dy's channels-last copy read by TMA boxes with element strides equal
+# to the stride).  Channel counts off the 64/128 tiles, odd extents, strides 1
+# to 4 (W stride 4: boxes 64 positions wide), 1-D and 3-D, dilation,
+# asymmetric pads, output_padding, 8 taps on an axis, a row wider than a tile.
+TC_DX = [
+    P("tcdx_2d_bf16", 2, 32, 48, (9, 12), 4, stride=2, pad=1, dtype="bf16", seed=3101),
+    P("tcdx_3d_f16", 1, 24, 40, (3, 6, 10), 3, stride=(1, 2, 2), pad=1, output_padding=(0, 1, 1),
+      dtype="f16", seed=3102),
+    P("tcdx_1d_dil", 3, 64, 16, (37,), 5, stride=3, pad_lo=(2,), pad_hi=(4,), dilation=2,
+      dtype="bf16", seed=3103),
+    P("tcdx_k8_s4", 1, 16, 130, (5, 7), 8, stride=4, pad=2, dtype="bf16", seed=3104),
+    P("tcdx_wide", 1, 80, 24, (3, 200), 3, stride=(1, 2), pad=1, output_padding=(0, 1), dtype="bf16",
+      seed=3105),
+    P("tcdx_s1", 2, 40, 72, (6, 7, 5), (2, 3, 2), stride=1, pad=(1, 0, 1), dtype="f16", seed=3106),
+]
+
+
+def test_backward_kernel_query_names_the_kernels_that_run():
+    """The query's answers on the workloads and on the shapes of each dx/dw
+    kernel class (the tensor-core dx on 16-bit problems of one group, the
+    small-group dw on groups of at most 8 channels)."""
+    def names(p):
+        return ct.ct_conv_transpose_backward_kernels(
+            p.B, p.C_in, p.C_out, p.spatial, p.k, p.stride, p.pad_lo, p.pad_hi, p.dilation,
+            p.output_padding, p.groups, ct.dtype_code(p.torch_dtype))
+    assert names(synth.workload(2)) == ("tc_phase_gemm", "bwd_dw_kernel")
+    assert names(synth.workload(4)) == ("tc_phase_gemm", "bwd_dw_kernel")
+    assert names(synth.workload(1)) == ("bwd_dx_kernel", "bwd_dw_kernel")
+    assert names(synth.workload(3)) == ("bwd_dx_kernel", "bwd_dw_grouped_kernel")
+    for p in TC_DX:
+        assert names(p)[0] == "tc_phase_gemm", p.name
+    for p in SMALL_GROUPS:
+        if p.name != "sg_36taps":
+            assert names(p)[1] == "bwd_dw_grouped_kernel", p.name
+
+
+@pytest.mark.parametrize("p", TC_DX, ids=lambda p: p.name)
+def test_backward_tensor_core_dx_matches_oracle(p):
+    x, w, _ = synth.make_inputs(p)
+    dy = _dy_for(p, 77)
+    rdx, _, _ = oracle.conv_transpose_backward(x, w, dy, **p.attrs(), need=("dx",))
+    dx, _, _ = _gpu_grads(p, x, w, dy, need=("dx",))
+    _check(p, dx, rdx, "dx")
+
+
 def test_grouped_dw_does_not_depend_on_pointer_alignment():
     """The small-group dw kernel stages fp32 rows by bulk copies widened to
     16-byte boundaries, so x and dy may start anywhere a float may: views one

@@ -15,6 +15,7 @@ from .ct import (  # noqa: F401
     ct_conv_transpose_workspace_bytes,
     ct_device_status, ct_host_buffers_release, ct_last_error, ct_status_string, ct_version,
     dtype_code, lib, ct_conv_transpose_backward_nd, ct_conv_transpose_backward_workspace_bytes,
+    ct_conv_transpose_backward_kernels,
     conv_transpose_backward, ConvTransposeFunction, conv_transpose_autograd,
     ct_conv_transpose_nd_ex, ct_conv_transpose_ex_workspace_bytes, ACTIVATIONS, CT_ACT_NONE,
     CT_ACT_RELU, CT_ACT_LEAKY_RELU, CT_ACT_SILU, CT_ACT_GELU, CT_ACT_TANH, CT_ACT_SIGMOID,

@@ -656,6 +656,24 @@ int ct_conv_transpose_backward_workspace_bytes(int nd, int64_t B, int64_t C_in, 
     return CT_OK;
 }
 
+int ct_conv_transpose_backward_kernels(int nd, int64_t B, int64_t C_in, int64_t C_out,
+                                       const int64_t* in_spatial, const int64_t* k, const int* stride,
+                                       const int* pad_lo, const int* pad_hi, const int* dilation,
+                                       const int* output_padding, int groups, int dtype,
+                                       const char** dx_kernel, const char** dw_kernel) {
+    Problem p;
+    int rc = validate(&p, nd, B, C_in, C_out, in_spatial, k, stride, pad_lo, pad_hi, dilation,
+                      output_padding, groups, dtype);
+    if (rc != CT_OK) return rc;
+    if (!dx_kernel || !dw_kernel) return fail(CT_ERR_NULL, "kernel name pointers must not be NULL");
+    if (!backward_supported(p))
+        return fail(CT_ERR_TOO_LARGE, "backward: %lld taps per input channel block exceed the staged slab",
+                    (long long)p.taps());
+    *dx_kernel = backward_dx_kernel_name(p);
+    *dw_kernel = backward_dw_kernel_name(p);
+    return CT_OK;
+}
+
 int ct_conv_transpose_backward_nd(const void* x, const void* w, const void* dy, void* dx, void* dw,
                                   void* db, void* workspace, size_t workspace_bytes, int nd,
                                   int64_t B, int64_t C_in, int64_t C_out,
@@ -677,7 +695,7 @@ int ct_conv_transpose_backward_nd(const void* x, const void* w, const void* dy, 
         return fail(CT_ERR_TOO_LARGE, "backward: %lld taps per input channel block exceed the staged slab",
                     (long long)p.taps());
     cudaStream_t s = (cudaStream_t)stream;
-    const size_t need = dw ? backward_workspace_bytes(p) : 0;
+    const size_t need = backward_workspace_bytes(p, dx != nullptr, dw != nullptr);
     void* ws = workspace;
     bool owned = false;
     if (need > 0) {

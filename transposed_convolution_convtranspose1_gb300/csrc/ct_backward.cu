@@ -48,6 +48,7 @@
 #include <type_traits>
 
 #include "ct_internal.h"
+#include "ct_routes.h"
 #include "ct_tcgen05.cuh"
 #include "ct_types.cuh"
 
@@ -1050,7 +1051,14 @@ cudaError_t launch_backward_t(const Problem& p, const BwdPlan& pl, BwdArgs a, cu
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    if (a.dx) {
+    if (a.dx && p.x_elems() > 0 && tc_dx_supports(p)) {
+        // tensor cores: dy's channels-last copy (with the gathered weights) in
+        // the workspace, then the GEMM; dw, if asked for, reuses the workspace
+        // after them on the same stream
+        e = launch_tc_dx(p, a.dy, a.w, a.dx, a.part, stream);
+        *launches += 2;
+        if (e != cudaSuccess) return e;
+    } else if (a.dx) {
         switch (pl.icb) {
             case 1: e = launch_dx_t<T, 1>(a, pl, stream); break;
             case 2: e = launch_dx_t<T, 2>(a, pl, stream); break;
@@ -1101,19 +1109,38 @@ cudaError_t backward_error_word(unsigned int* v, bool clear) {
     return e;
 }
 
+const char* backward_dx_kernel_name(const Problem& p) {
+    if (p.x_elems() == 0) return "";
+    return tc_dx_supports(p) ? "tc_phase_gemm" : "bwd_dx_kernel";
+}
+
+const char* backward_dw_kernel_name(const Problem& p) {
+    if (p.w_elems() == 0) return "";
+    DeviceInfo d;
+    int sm = 152;
+    if (device_info(&d) == cudaSuccess) sm = d.sm_count;
+    BwdPlan pl;
+    if (!bwd_plan(p, sm, &pl)) return "";
+    return pl.dwg ? "bwd_dw_grouped_kernel" : "bwd_dw_kernel";
+}
+
 bool backward_supported(const Problem& p) {
     BwdPlan pl;
     return bwd_plan(p, 152, &pl);
 }
 
-size_t backward_workspace_bytes(const Problem& p) {
+size_t backward_workspace_bytes(const Problem& p, bool dx, bool dw) {
     DeviceInfo d;
     int sm = 152;
     if (device_info(&d) == cudaSuccess) sm = d.sm_count;
     BwdPlan pl;
     if (!bwd_plan(p, sm, &pl)) return 0;
-    return (pl.part_bytes + 255) / 256 * 256;
+    size_t need = dw ? (pl.part_bytes + 255) / 256 * 256 : 0;
+    if (dx && p.x_elems() > 0 && tc_dx_supports(p)) need = std::max(need, tc_dx_workspace_bytes(p));
+    return need;
 }
+
+size_t backward_workspace_bytes(const Problem& p) { return backward_workspace_bytes(p, true, true); }
 
 cudaError_t launch_backward(const Problem& p, const void* x, const void* w, const void* dy, void* dx,
                             void* dw, void* db, void* workspace, cudaStream_t stream, int* launches) {

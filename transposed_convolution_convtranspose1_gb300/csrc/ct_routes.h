@@ -60,7 +60,19 @@ cudaError_t launch_tc32(const Problem& p, const void* x, const void* w, const vo
 // dx, dw and db, each skipped when its pointer is null.  The workspace holds
 // dw's per-slice fp32 partials.  `launches` (optional) counts the kernels.
 bool backward_supported(const Problem& p);
+// Workspace of the backward call: the larger of the dw partials and, when dx
+// runs on the tensor cores, dy's channels-last copy and the gathered weights
+// (stream-ordered, so the two uses share it).
 size_t backward_workspace_bytes(const Problem& p);
+size_t backward_workspace_bytes(const Problem& p, bool dx, bool dw);
+// Kernels that take most of the device time of dx and of dw.
+const char* backward_dx_kernel_name(const Problem& p);
+const char* backward_dw_kernel_name(const Problem& p);
+// The input gradient on the tcgen05 GEMM (16-bit types, groups of 1): ct_tc.cu.
+bool tc_dx_supports(const Problem& p);
+size_t tc_dx_workspace_bytes(const Problem& p);
+cudaError_t launch_tc_dx(const Problem& p, const void* dy, const void* w, void* dx, void* workspace,
+                         cudaStream_t stream);
 cudaError_t launch_backward(const Problem& p, const void* x, const void* w, const void* dy, void* dx,
                             void* dw, void* db, void* workspace, cudaStream_t stream, int* launches);
 

@@ -91,6 +91,7 @@ struct TcParams {
     int ntap[3][kTcMaxS];
     int tap[3][kTcMaxS][kTcMaxTaps];
     int off[3][kTcMaxS][kTcMaxTaps];
+    int cmul[3];          // X' coordinate of tile position q on each axis: q * cmul + tap offset
     int n_classes, total_tiles;
     int g_qd, g_qh, g_qw;   // spatial tile grid (largest over the classes)
     TcClass cls[kTcMaxClasses];
@@ -276,9 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_phase_gemm(const __grid_consta
                             const int tap = (P.tap[0][tl.rd][jd] * P.Kdims[1] + P.tap[1][tl.rh][jh]) *
                                                 P.Kdims[2] +
                                             P.tap[2][rw][jw];
-                            const int id = tl.qd + P.off[0][tl.rd][jd];
-                            const int ih = tl.qh0 + P.off[1][tl.rh][jh];
-                            const int iw = tl.qw0 + P.off[2][rw][jw];
+                            const int id = tl.qd * P.cmul[0] + P.off[0][tl.rd][jd];
+                            const int ih = tl.qh0 * P.cmul[1] + P.off[1][tl.rh][jh];
+                            const int iw = tl.qw0 * P.cmul[2] + P.off[2][rw][jw];
                             for (int kb = 0; kb < P.n_kblk; ++kb) {
                                 ok = issued < (uint32_t)P.stages ||  // a fresh slot is free
                                      __all_sync(0xffffffffu,
@@ -642,8 +643,9 @@ struct TcPrep {
     int C, C_pad, B, C_out, taps, N_pad;
     int64_t S;
     int n_st, n_ct, n_jt;  // x tiles along s and c; weight tiles along j
-    int64_t n_wb;          // weight tiles (first blocks of the grid)
+    int64_t n_wb;          // weight blocks (first blocks of the grid)
     bool vec;
+    bool w_gather;         // W'[tap][n][c] = w[n][c][tap] (input gradient), 256 elements per block
 };
 
 template <typename T>
@@ -651,7 +653,18 @@ __global__ void __launch_bounds__(256) tc_prepare(const __grid_constant__ TcPrep
     // the GEMM that follows may begin its prologue now
     asm volatile("griddepcontrol.launch_dependents;");
     const int64_t bid = blockIdx.x;
-    if (bid < Q.n_wb) {
+    if (bid < Q.n_wb && Q.w_gather) {
+        // input gradient: W'[tap][n][c] = w[n][c][tap] (n < C_out, c < C, else 0); w is small
+        const int64_t e = bid * 256 + threadIdx.x;
+        const int64_t plane = (int64_t)Q.N_pad * Q.C_pad;
+        if (e < plane * Q.taps) {
+            const int tp = (int)(e / plane);
+            const int n = (int)((e / Q.C_pad) % Q.N_pad), c = (int)(e % Q.C_pad);
+            const uint16_t* ws = static_cast<const uint16_t*>(Q.w);
+            static_cast<uint16_t*>(Q.wp)[e] =
+                n < Q.C_out && c < Q.C ? ws[((int64_t)n * Q.C + c) * Q.taps + tp] : (uint16_t)0;
+        }
+    } else if (bid < Q.n_wb) {
         const int64_t wb = bid;
         const int jt = (int)(wb % Q.n_jt), ct = (int)(wb / Q.n_jt);
         tc_weight_tile<T>(static_cast<const T*>(Q.w), static_cast<T*>(Q.wp), Q.C, Q.C_out, Q.taps,
@@ -739,10 +752,20 @@ cudaError_t launch_gemm(const TcParams& P, int grid, size_t smem, cudaStream_t s
                       : launch_gemm_t<T, SW, false>(P, grid, smem, stream);
 }
 
+// How the GEMM reads its operands when it computes an input gradient instead
+// of the forward pass: X' coordinates q * cmul + offset, X' boxes that take
+// every es-th position on W and H (TMA element strides), W' gathered as
+// w[n][c][tap].
+struct TcOperands {
+    int cmul[3];
+    int es_w, es_h;
+    bool w_gather;
+};
+
 template <typename T>
 cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const void* w,
                         const void* bias, void* y, void* workspace, cudaStream_t stream,
-                        Profile* prof) {
+                        Profile* prof, const TcOperands* ops = nullptr) {
     DeviceInfo dev;
     cudaError_t e = device_info(&dev);
     if (e != cudaSuccess) return e;
@@ -759,6 +782,7 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
     P.act_alpha = p.act_alpha;
     P.y = y;
     P.C_out = (int)p.C_out;
+    for (int a = 0; a < 3; ++a) P.cmul[a] = ops ? ops->cmul[a] : 1;
     P.n_kblk = pl.C_pad / kBlockK;
     P.n_oc_tiles = pl.n_oc_tiles;
     for (int a = 0; a < 3; ++a) {
@@ -862,8 +886,10 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
         const cuuint64_t row = (cuuint64_t)pl.C_pad * 2;
         const cuuint64_t strides[4] = {row, row * p.I[2], row * p.I[2] * p.I[1],
                                        row * p.I[2] * p.I[1] * p.I[0]};
-        const cuuint32_t box[5] = {(cuuint32_t)kBlockK, (cuuint32_t)pl.WC, (cuuint32_t)pl.MR, 1, 1};
-        const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+        // with element strides the box spans es x the positions it loads
+        const cuuint32_t esw = ops ? (cuuint32_t)ops->es_w : 1u, esh = ops ? (cuuint32_t)ops->es_h : 1u;
+        const cuuint32_t box[5] = {(cuuint32_t)kBlockK, (cuuint32_t)pl.WC * esw, (cuuint32_t)pl.MR * esh, 1, 1};
+        const cuuint32_t es[5] = {1, esw, esh, 1, 1};
         CUresult r = enc(&P.tmap_x, dt, 5, xc, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -895,6 +921,8 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
         Q.n_ct = pl.C_pad / 64;
         Q.n_jt = (int)(((int64_t)pl.N_pad * p.taps() + 63) / 64);
         Q.n_wb = (int64_t)Q.n_jt * Q.n_ct;
+        Q.w_gather = ops && ops->w_gather;
+        if (Q.w_gather) Q.n_wb = ((int64_t)p.taps() * pl.N_pad * pl.C_pad + 255) / 256;
         // 16-byte loads need S % 8 == 0 and a 16-byte aligned x
         Q.vec = (Q.S % 8) == 0 && ((uintptr_t)x % 16) == 0;
         const int64_t blocks = Q.n_wb + (int64_t)Q.n_st * Q.n_ct * p.B;
@@ -917,7 +945,96 @@ cudaError_t launch_tc_t(const Problem& p, const TcPlan& pl, const void* x, const
     return e;
 }
 
+// The input gradient as a GEMM on this kernel (groups of 1, 16-bit types):
+//     dx[b, ic, i] = sum_{oc, t} w[ic, oc, t] * dy[b, oc, i * s + t * d - pad_lo]
+// is the kernel's computation with one output phase (stride 1), the input
+// gradient's channels as output channels, dy's channels as the reduction, all
+// taps of every axis at X' offsets t * d - pad_lo, and the tile position q of
+// an axis mapped to X' coordinate q * s: X' is the channels-last copy of dy,
+// read with TMA element strides s on W and H (on D a box is one position, so
+// the coordinate alone does it).  W' gathers w[ic][oc][t] into [t][ic][oc].
+// Fills the GEMM's problem and plan; false when the shape is off this route.
+bool make_plan_dx(const Problem& p, TcPlan* pl, Problem* pd, TcOperands* ops) {
+    if (p.dtype != CT_BF16 && p.dtype != CT_F16) return false;
+    if (p.G != 1) return false;
+    for (int a = 0; a < 3; ++a)
+        if (p.K[a] > kTcMaxTaps || p.S[a] > 8) return false;
+    *pd = p;
+    pd->C_in = p.C_out;
+    pd->C_out = p.C_in;
+    pd->Cig = (int)pd->C_in;
+    pd->Cog = (int)pd->C_out;
+    pd->act = 0;
+    for (int a = 0; a < 3; ++a) {
+        pd->I[a] = p.O[a];
+        pd->O[a] = p.I[a];
+        pd->S[a] = 1;
+        AxisPlan& ax = pl->ax[a];
+        std::memset(&ax, 0, sizeof(ax));
+        ax.s = 1;
+        ax.q_extent[0] = p.I[a];
+        ax.ntaps[0] = (int)p.K[a];
+        for (int j = 0; j < p.K[a]; ++j) {
+            ax.tap[0][j] = j;
+            ax.off[0][j] = j * p.DL[a] - p.PL[a];
+        }
+        ops->cmul[a] = p.S[a];
+    }
+    ops->es_w = p.S[2];
+    ops->es_h = p.S[1];
+    ops->w_gather = true;
+    pl->sw = 1;
+    pl->NP = 256;
+    pl->nslot = 2;
+    pl->N_pad = (int)((pd->C_out + kBlockM - 1) / kBlockM * kBlockM);
+    pl->n_oc_tiles = pl->N_pad / kBlockM;
+    pl->C_pad = (int)((pd->C_in + kBlockK - 1) / kBlockK * kBlockK);
+    int wc = 32;  // an epilogue chunk (32 positions) stays within one row
+    while (wc < p.I[2] && wc < pl->NP && wc * 2 * p.S[2] <= 256) wc *= 2;
+    pl->WC = wc;
+    pl->MR = pl->NP / wc;
+    if (wc * p.S[2] > 256 || pl->MR * p.S[1] > 256) return false;  // TMA box extents
+    pl->stage_bytes = (size_t)kBlockM * 128 + (size_t)pl->NP * 128;
+    pl->epi_bytes = 0;
+    pl->stages = (int)std::min<size_t>(8, (kSmemLimit - 2048) / pl->stage_bytes);
+    if (pl->stages < 2) return false;
+    pl->x_bytes = (size_t)p.B * p.out_spatial() * pl->C_pad * 2;
+    pl->w_bytes = (size_t)p.taps() * pl->N_pad * pl->C_pad * 2;
+    if ((double)p.out_spatial() * pl->C_pad * 2 * p.B >= 1e12) return false;
+    return true;
+}
+
 }  // namespace
+
+bool tc_dx_supports(const Problem& p) {
+    TcPlan pl;
+    Problem pd;
+    TcOperands ops;
+    if (!make_plan_dx(p, &pl, &pd, &ops)) return false;
+    if (p.C_in < 16 || p.C_out < 16) return false;  // tiny channel counts: the CUDA-core kernel
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess) return false;
+    return d.cc_major == 10 && d.cc_minor == 3;
+}
+
+size_t tc_dx_workspace_bytes(const Problem& p) {
+    TcPlan pl;
+    Problem pd;
+    TcOperands ops;
+    if (!make_plan_dx(p, &pl, &pd, &ops)) return 0;
+    return round256(pl.x_bytes) + round256(pl.w_bytes);
+}
+
+cudaError_t launch_tc_dx(const Problem& p, const void* dy, const void* w, void* dx, void* workspace,
+                         cudaStream_t stream) {
+    TcPlan pl;
+    Problem pd;
+    TcOperands ops;
+    if (!make_plan_dx(p, &pl, &pd, &ops)) return cudaErrorInvalidValue;
+    if (p.dtype == CT_BF16)
+        return launch_tc_t<__nv_bfloat16>(pd, pl, dy, w, nullptr, dx, workspace, stream, nullptr, &ops);
+    return launch_tc_t<__half>(pd, pl, dy, w, nullptr, dx, workspace, stream, nullptr, &ops);
+}
 
 bool tc_supports(const Problem& p) {
     TcPlan pl;

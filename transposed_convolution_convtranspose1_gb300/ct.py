@@ -51,6 +51,7 @@ EXPORTS = ("ct_version", "ct_last_error", "ct_status_string",
            "ct_conv_transpose_nd_host", "ct_conv_transpose_nd_profiled",
            "ct_conv_transpose_nd_noalloc", "ct_device_status", "ct_host_buffers_release",
            "ct_conv_transpose_backward_nd", "ct_conv_transpose_backward_workspace_bytes",
+           "ct_conv_transpose_backward_kernels",
            "ct_conv_transpose_nd_ex", "ct_conv_transpose_ex_workspace_bytes",
            "ct_set_wait_limit_ns")
 
@@ -105,6 +106,8 @@ def _declare(h):
     h.ct_conv_transpose_route.argtypes = _SHAPE_ARGS + [_i32p]
     h.ct_conv_transpose_kernel.restype = ctypes.c_int
     h.ct_conv_transpose_kernel.argtypes = _SHAPE_ARGS + [ctypes.POINTER(ctypes.c_char_p)]
+    h.ct_conv_transpose_backward_kernels.restype = ctypes.c_int
+    h.ct_conv_transpose_backward_kernels.argtypes = _SHAPE_ARGS + [ctypes.POINTER(ctypes.c_char_p)] * 2
     h.ct_conv_transpose_nd.restype = ctypes.c_int
     h.ct_conv_transpose_nd.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_size_t] + _SHAPE_ARGS + [_vp]
     h.ct_conv_transpose_nd_route.restype = ctypes.c_int
@@ -249,6 +252,17 @@ def ct_conv_transpose_kernel(B, C_in, C_out, in_spatial, k, stride=None, pad_lo=
     _check(lib().ct_conv_transpose_kernel(*_shape_args(B, C_in, C_out, ax, groups, dtype),
                                           ctypes.byref(name)))
     return name.value.decode() if name.value is not None else ""
+
+
+def ct_conv_transpose_backward_kernels(B, C_in, C_out, in_spatial, k, stride=None, pad_lo=None,
+                                       pad_hi=None, dilation=None, output_padding=None, groups=1,
+                                       dtype=CT_F32):
+    """Names of the kernels that dominate the input and weight gradients' device time: (dx, dw)."""
+    ax = _Axes(len(in_spatial), in_spatial, k, stride, pad_lo, pad_hi, dilation, output_padding)
+    dx, dw = ctypes.c_char_p(), ctypes.c_char_p()
+    _check(lib().ct_conv_transpose_backward_kernels(*_shape_args(B, C_in, C_out, ax, groups, dtype),
+                                                    ctypes.byref(dx), ctypes.byref(dw)))
+    return tuple(n.value.decode() if n.value is not None else "" for n in (dx, dw))
 
 
 def _ptr(t: Optional[torch.Tensor]):
