@@ -567,7 +567,7 @@ def backward_per_config(dev, flush, peaks):
                 nbytes = dy.numel() * dy.element_size() + p.C_out * dy.element_size()
                 ach = nbytes / (ms * 1e-3) / 1e9
                 res[name] = [round(ms, 5), round(ach / peaks["hbm_gbs"], 4)]
-            elif kern[name] == "tc_phase_gemm":
+            elif kern[name] in ("tc_phase_gemm", "tc_dw_gemm"):
                 ach = flops / (ms * 1e-3) / 1e12
                 res[name] = [round(ms, 5), round(ach / peaks["bf16_tflops"], 4), "t"]
             else:

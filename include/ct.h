@@ -376,9 +376,11 @@ int ct_conv_transpose_backward_workspace_bytes(int nd, int64_t B, int64_t C_in,
  * gradient and of the weight gradient of ct_conv_transpose_backward_nd on
  * this problem, written to *dx_kernel and *dw_kernel as pointers to static
  * strings: "tc_phase_gemm" (dx on the tensor cores: bf16/fp16, groups of 1,
- * at least 16 channels each side) or "bwd_dx_kernel"; "bwd_dw_grouped_kernel"
- * (groups of at most 8 input and 8 output channels, at most 27 taps) or
- * "bwd_dw_kernel"; "" for an empty gradient.  Host only; depends on the
+ * at least 16 channels each side) or "bwd_dx_kernel"; "tc_dw_gemm" (dw on
+ * the tensor cores: the same class with a W stride of at most 4 and an input
+ * width that is a multiple of 8), "bwd_dw_grouped_kernel" (groups of at most
+ * 8 input and 8 output channels, at most 27 taps) or "bwd_dw_kernel"; "" for
+ * an empty gradient.  Host only; depends on the
  * current device.  Errors as ct_conv_transpose_backward_workspace_bytes.
  */
 int ct_conv_transpose_backward_kernels(int nd, int64_t B, int64_t C_in,

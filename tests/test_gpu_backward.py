@@ -160,15 +160,44 @@ def test_backward_kernel_query_names_the_kernels_that_run():
         return ct.ct_conv_transpose_backward_kernels(
             p.B, p.C_in, p.C_out, p.spatial, p.k, p.stride, p.pad_lo, p.pad_hi, p.dilation,
             p.output_padding, p.groups, ct.dtype_code(p.torch_dtype))
-    assert names(synth.workload(2)) == ("tc_phase_gemm", "bwd_dw_kernel")
-    assert names(synth.workload(4)) == ("tc_phase_gemm", "bwd_dw_kernel")
+    assert names(synth.workload(2)) == ("tc_phase_gemm", "tc_dw_gemm")
+    assert names(synth.workload(4)) == ("tc_phase_gemm", "tc_dw_gemm")
     assert names(synth.workload(1)) == ("bwd_dx_kernel", "bwd_dw_kernel")
     assert names(synth.workload(3)) == ("bwd_dx_kernel", "bwd_dw_grouped_kernel")
     for p in TC_DX:
         assert names(p)[0] == "tc_phase_gemm", p.name
+    for p in TC_DW:
+        assert names(p)[1] == "tc_dw_gemm", p.name
     for p in SMALL_GROUPS:
         if p.name != "sg_36taps":
             assert names(p)[1] == "bwd_dw_grouped_kernel", p.name
+
+
+# dw on the tcgen05 GEMM (16-bit, one group, >= 16 channels, W stride <= 4,
+# input width a multiple of 8): x K-major from its own layout, dy MN-major from
+# its channels-last copy read with element strides; several input- and
+# output-channel blocks and tap pairs (an odd tap count), rows longer than a
+# 64-position block, 1-D and 3-D, dilation, asymmetric pads, W stride 4.
+TC_DW = [
+    P("tcdw_2d", 2, 32, 48, (9, 16), 4, stride=2, pad=1, dtype="bf16", seed=3201),
+    P("tcdw_3d_f16", 1, 24, 40, (3, 6, 16), 3, stride=(1, 2, 2), pad=1, output_padding=(0, 1, 1),
+      dtype="f16", seed=3202),
+    P("tcdw_1d_dil", 3, 64, 16, (40,), 5, stride=3, pad_lo=(2,), pad_hi=(4,), dilation=2,
+      dtype="bf16", seed=3203),
+    P("tcdw_wide", 1, 80, 24, (3, 200), 3, stride=(1, 2), pad=1, output_padding=(0, 1), dtype="bf16",
+      seed=3204),
+    P("tcdw_blocks", 1, 160, 136, (4, 8), 2, stride=2, dtype="bf16", seed=3205),
+    P("tcdw_s4", 1, 16, 130, (5, 8), 8, stride=4, pad=2, dtype="bf16", seed=3206),
+]
+
+
+@pytest.mark.parametrize("p", TC_DW, ids=lambda p: p.name)
+def test_backward_tensor_core_dw_matches_oracle(p):
+    x, w, _ = synth.make_inputs(p)
+    dy = _dy_for(p, 78)
+    _, rdw, _ = oracle.conv_transpose_backward(x, w, dy, **p.attrs(), need=("dw",))
+    _, dw, _ = _gpu_grads(p, x, w, dy, need=("dw",))
+    _check(p, dw, rdw, "dw")
 
 
 @pytest.mark.parametrize("p", TC_DX, ids=lambda p: p.name)

@@ -1070,7 +1070,13 @@ cudaError_t launch_backward_t(const Problem& p, const BwdPlan& pl, BwdArgs a, cu
         if (e != cudaSuccess) return e;
     }
     const int64_t nw = p.w_elems();
-    if (a.dw && nw > 0 && pl.dwg) {
+    if (a.dw && nw > 0 && p.B * p.in_spatial() > 0 && tc_dw_supports(p) && (uintptr_t)a.x % 16 == 0) {
+        // tensor cores: dy's channels-last copy and the split partials in the
+        // workspace, then the GEMM and the reduction of the splits
+        e = launch_tc_dw(p, a.x, a.dy, a.dw, a.part, stream);
+        *launches += 3;
+        if (e != cudaSuccess) return e;
+    } else if (a.dw && nw > 0 && pl.dwg) {
         const int64_t blocks = (int64_t)p.G * pl.n_ks;
         switch (pl.dwg_kn) {
             case 4: e = launch_dwg_t<T, 8, 4>(a, pl, blocks, stream); break;
@@ -1121,6 +1127,7 @@ const char* backward_dw_kernel_name(const Problem& p) {
     if (device_info(&d) == cudaSuccess) sm = d.sm_count;
     BwdPlan pl;
     if (!bwd_plan(p, sm, &pl)) return "";
+    if (tc_dw_supports(p) && p.B * p.in_spatial() > 0) return "tc_dw_gemm";
     return pl.dwg ? "bwd_dw_grouped_kernel" : "bwd_dw_kernel";
 }
 
@@ -1136,6 +1143,7 @@ size_t backward_workspace_bytes(const Problem& p, bool dx, bool dw) {
     BwdPlan pl;
     if (!bwd_plan(p, sm, &pl)) return 0;
     size_t need = dw ? (pl.part_bytes + 255) / 256 * 256 : 0;
+    if (dw && p.w_elems() > 0 && tc_dw_supports(p)) need = std::max(need, tc_dw_workspace_bytes(p));
     if (dx && p.x_elems() > 0 && tc_dx_supports(p)) need = std::max(need, tc_dx_workspace_bytes(p));
     return need;
 }

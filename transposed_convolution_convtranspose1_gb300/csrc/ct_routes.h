@@ -73,6 +73,11 @@ bool tc_dx_supports(const Problem& p);
 size_t tc_dx_workspace_bytes(const Problem& p);
 cudaError_t launch_tc_dx(const Problem& p, const void* dy, const void* w, void* dx, void* workspace,
                          cudaStream_t stream);
+// The weight gradient on the tcgen05 GEMM (16-bit types, groups of 1): ct_tc.cu.
+bool tc_dw_supports(const Problem& p);
+size_t tc_dw_workspace_bytes(const Problem& p);
+cudaError_t launch_tc_dw(const Problem& p, const void* x, const void* dy, void* dw, void* workspace,
+                         cudaStream_t stream);
 cudaError_t launch_backward(const Problem& p, const void* x, const void* w, const void* dy, void* dx,
                             void* dw, void* db, void* workspace, cudaStream_t stream, int* launches);
 

@@ -680,6 +680,229 @@ __global__ void __launch_bounds__(256) tc_prepare(const __grid_constant__ TcPrep
 }
 
 // ---------------------------------------------------------------------------
+// the weight gradient as a GEMM (16-bit types, groups of 1)
+//
+// Per tap t, dw_t[ic, oc] = sum over (b, i) of x[b, ic, i] * dy[b, oc, i * s +
+// t * d - pad_lo]: M = 128 input channels, N = 128 output channels, K = input
+// positions, 64 per k-block (one run of an input row).  A (x) is K-major
+// straight from x's layout; B (dy at the tap's positions) is MN-major, from
+// dy's channels-last copy: a box of 64 output channels x 64 positions taken
+// with element stride s_W (so a tap's shift lands on a non-innermost
+// coordinate, as TMA requires), two boxes for the 128 channels.  A tile
+// keeps kDwNT taps in TMEM so that each A block serves them all.  The k-blocks
+// are split over about one wave of CTAs; each writes fp32 partials
+// [split][tap][ic][oc] and tc_dw_reduce adds the splits in order.
+// ---------------------------------------------------------------------------
+
+constexpr int kDwNT = 2;          // taps per tile
+constexpr int kDwThreads = 192;   // producer, MMA, four epilogue warps
+
+struct TcDwParams {
+    CUtensorMap tmap_x;   // x [B, C_in, I_D, I_H, I_W] as 5-D (I_W, I_H, I_D, C_in, B)
+    CUtensorMap tmap_dy;  // dy' [B, O_D, O_H, O_W, C_pad] as 5-D (C_pad, O_W, O_H, O_D, B)
+    float* part;          // [split][tap][C_in][C_out]
+    int C_in, C_out, taps;
+    int I[3], K[3], S[3], PL[3], DL[3];
+    int n_icb, n_ocb, n_tg;   // tiles: input-channel blocks, output-channel blocks, tap groups
+    int n_wblk;               // 64-position blocks per input row
+    int64_t n_kb;             // k-blocks: B * I_D * I_H * n_wblk
+    int n_split;
+    int stages;
+    uint32_t idesc;
+    uint64_t wait_ns;
+};
+
+// Shared-memory matrix descriptor: MN-major, 128-byte swizzle: rows of 64
+// MN elements (128 bytes) per K index, 8-row groups 1024 bytes apart along K
+// (SBO), 64-element MN blocks 8192 bytes apart (LBO), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);       // start address
+    d |= (uint64_t)(8192u >> 4) << 16;             // leading byte offset: next 64 MN elements
+    d |= (uint64_t)(1024u >> 4) << 32;             // stride byte offset: next 8 K rows
+    d |= (uint64_t)1 << 46;                        // version
+    d |= (uint64_t)2 << 61;                        // SWIZZLE_128B
+    return d;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kDwThreads, 1) tc_dw_gemm(const __grid_constant__ TcDwParams P) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint64_t full_bar[8], empty_bar[8], done_bar;
+    __shared__ uint32_t tmem_base_slot;
+    __shared__ volatile int abort_flag;
+    constexpr uint32_t kA = 128 * 128;        // A block: 128 channels x 64 positions x 2 bytes
+    constexpr uint32_t kB = 128 * 128;        // B block of one tap: two 64 x 64 boxes
+    constexpr uint32_t kStage = kA + kDwNT * kB;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int n_tiles = P.n_icb * P.n_ocb * P.n_tg;
+    const int tile = (int)(blockIdx.x % n_tiles), split = (int)(blockIdx.x / n_tiles);
+    const int tg = tile % P.n_tg, ocb = (tile / P.n_tg) % P.n_ocb, icb = tile / (P.n_tg * P.n_ocb);
+    const int64_t kb0 = (int64_t)split * P.n_kb / P.n_split, kb1 = (int64_t)(split + 1) * P.n_kb / P.n_split;
+    const int t0 = tg * kDwNT, nt = min(kDwNT, P.taps - t0);
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < P.stages; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        mbar_init(smem_u32(&done_bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_x)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_dy)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&tmem_base_slot)),
+                     "r"(kDwNT * 128u)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_base_slot;
+    // dy' comes from the preceding prepare kernel (launched as its programmatic dependent)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int stage = 0;
+        uint32_t phase = 0, issued = 0;
+        bool ok = true;
+        for (int64_t kb = kb0; kb < kb1 && ok; ++kb) {
+            ok = issued < (uint32_t)P.stages ||
+                 __all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, kErrProducer,
+                                                   &abort_flag, P.wait_ns));
+            if (!ok) break;
+            if (lane == 0) {
+                int64_t r = kb;
+                const int wb = (int)(r % P.n_wblk); r /= P.n_wblk;
+                const int i1 = (int)(r % P.I[1]); r /= P.I[1];
+                const int i0 = (int)(r % P.I[0]);
+                const int b = (int)(r / P.I[0]);
+                const uint32_t fb = smem_u32(&full_bar[stage]);
+                const uint32_t sa = ring + stage * kStage;
+                mbar_expect_tx(fb, kA + nt * kB);
+                tma_load_5d(sa, &P.tmap_x, fb, wb * 64, i1, i0, icb * 128, b);
+                for (int j = 0; j < nt; ++j) {
+                    const int t = t0 + j;
+                    const int td = t / (P.K[1] * P.K[2]), th = (t / P.K[2]) % P.K[1], tw = t % P.K[2];
+                    const int cw = wb * 64 * P.S[2] + tw * P.DL[2] - P.PL[2];
+                    const int ch = i1 * P.S[1] + th * P.DL[1] - P.PL[1];
+                    const int cd = i0 * P.S[0] + td * P.DL[0] - P.PL[0];
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_5d(sa + kA + j * kB + h * 8192u, &P.tmap_dy, fb, ocb * 128 + h * 64, cw, ch, cd,
+                                    b);
+                }
+            }
+            __syncwarp();
+            ++issued;
+            if (++stage == P.stages) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+        if (!ok && lane == 0) {
+            const uint32_t first = issued > (uint32_t)P.stages ? issued - P.stages : 0;
+            for (uint32_t k = first; k < issued; ++k)
+                mbar_drain(smem_u32(&full_bar[k % P.stages]), (k / P.stages) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int64_t kb = kb0; kb < kb1 && ok; ++kb) {
+                if (!mbar_wait(smem_u32(&full_bar[stage]), phase, kErrMma, &abort_flag, P.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = ring + stage * kStage;
+                const uint64_t ad = smem_desc_sw128(sa);
+                for (int j = 0; j < nt; ++j) {
+                    const uint64_t bd = smem_desc_mn_sw128(sa + kA + j * kB);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)  // K = 16 per MMA: A +32 bytes, B +16 rows (2048 bytes)
+                        mma_f16(tmem_base + j * 128, ad + 2 * k, bd + 128 * k, P.idesc,
+                                (kb > kb0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(smem_u32(&empty_bar[stage]));
+                if (++stage == P.stages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            mma_commit(smem_u32(&done_bar));  // every MMA issued has completed when it fires
+            mbar_drain(smem_u32(&done_bar), 0);  // none may be in flight when TMEM is released
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        // warp w reads TMEM lane quarter q = w % 4: input channels icb*128 + 32q + lane
+        const int q = warp & 3;
+        const bool ok = __all_sync(0xffffffffu,
+                                   mbar_wait(smem_u32(&done_bar), 0, kErrEpilogue, &abort_flag, P.wait_ns));
+        if (ok) {
+            tc_fence_after();
+            const int ic = icb * 128 + q * 32 + lane;
+            const bool any = kb1 > kb0;  // an empty k range leaves TMEM unwritten: its partial is 0
+            for (int j = 0; j < nt; ++j) {
+                float* dst = P.part + (((int64_t)split * P.taps + t0 + j) * P.C_in + ic) * P.C_out;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float v[32];
+                    if (any) {
+                        tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * 128 + c * 32), v);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                    }
+                    const int oc0 = ocb * 128 + c * 32;
+                    if (ic < P.C_in)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (oc0 + i < P.C_out) dst[oc0 + i] = v[i];
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kDwNT * 128u)
+                     : "memory");
+    }
+}
+
+// dw[ic][oc][t] = sum over splits (in order) of part[split][t][ic][oc], one rounding.
+template <typename T>
+__global__ void __launch_bounds__(256) tc_dw_reduce(const float* __restrict__ part, T* __restrict__ dw, int C_in,
+                                                     int C_out, int taps, int n_split) {
+    const int64_t n = (int64_t)taps * C_in * C_out;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
+        float s = 0.f;
+#pragma unroll 4
+        for (int k = 0; k < n_split; ++k) s += part[(int64_t)k * n + e];
+        const int oc = (int)(e % C_out);
+        const int64_t r = e / C_out;
+        const int ic = (int)(r % C_in), t = (int)(r / C_in);
+        dw[((int64_t)ic * C_out + oc) * taps + t] = from_f32<T>(s);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host planning
 // ---------------------------------------------------------------------------
 
@@ -1004,7 +1227,175 @@ bool make_plan_dx(const Problem& p, TcPlan* pl, Problem* pd, TcOperands* ops) {
     return true;
 }
 
+struct DwPlan {
+    int C_pad, n_icb, n_ocb, n_tg, n_wblk, n_split, stages;
+    int64_t n_kb;
+    size_t x_bytes, part_bytes;
+};
+
+// The weight gradient's GEMM plan (16-bit types, groups of 1, at least 16
+// channels each side, W stride at most 4 so a B box spans at most 256
+// positions, I_W a multiple of 8 so x's rows are 16-byte strided for TMA).
+// The k-blocks are split so that the tiles x splits fill about one wave of
+// one CTA per SM.
+bool make_plan_dw(const Problem& p, int sm_count, DwPlan* pl) {
+    if (p.dtype != CT_BF16 && p.dtype != CT_F16) return false;
+    if (p.G != 1 || p.C_in < 16 || p.C_out < 16) return false;
+    if (p.S[2] > 4 || p.I[2] % 8 != 0) return false;
+    pl->C_pad = (int)((p.C_out + kBlockK - 1) / kBlockK * kBlockK);
+    pl->n_icb = (int)((p.C_in + 127) / 128);
+    pl->n_ocb = (int)((p.C_out + 127) / 128);
+    pl->n_tg = (int)((p.taps() + kDwNT - 1) / kDwNT);
+    pl->n_wblk = (int)((p.I[2] + 63) / 64);
+    pl->n_kb = p.B * p.I[0] * p.I[1] * pl->n_wblk;
+    const int64_t tiles = (int64_t)pl->n_icb * pl->n_ocb * pl->n_tg;
+    const int64_t split = std::max<int64_t>(1, std::min<int64_t>(std::max<int64_t>(1, pl->n_kb),
+                                                                  std::max(1, sm_count) / std::max<int64_t>(1, tiles)));
+    pl->n_split = (int)split;
+    if (tiles * split >= (1ll << 31)) return false;
+    pl->stages = (int)std::min<size_t>(8, (kSmemLimit - 2048) / (size_t)(128 * 128 * (1 + kDwNT)));
+    pl->x_bytes = (size_t)p.B * p.out_spatial() * pl->C_pad * 2;
+    pl->part_bytes = (size_t)split * p.taps() * p.C_in * p.C_out * sizeof(float);
+    if ((double)p.out_spatial() * pl->C_pad * 2 * p.B >= 1e12) return false;
+    return true;
+}
+
+template <typename T>
+cudaError_t launch_tc_dw_t(const Problem& p, const DwPlan& pl, const void* x, const void* dy, void* dw,
+                           void* workspace, cudaStream_t stream) {
+    char* ws = static_cast<char*>(workspace);
+    T* dyc = reinterpret_cast<T*>(ws);
+    float* part = reinterpret_cast<float*>(ws + round256(pl.x_bytes));
+    TcDwParams P;
+    std::memset(&P, 0, sizeof(P));
+    P.part = part;
+    P.C_in = (int)p.C_in;
+    P.C_out = (int)p.C_out;
+    P.taps = (int)p.taps();
+    for (int a = 0; a < 3; ++a) {
+        P.I[a] = (int)p.I[a];
+        P.K[a] = (int)p.K[a];
+        P.S[a] = p.S[a];
+        P.PL[a] = p.PL[a];
+        P.DL[a] = p.DL[a];
+    }
+    P.n_icb = pl.n_icb;
+    P.n_ocb = pl.n_ocb;
+    P.n_tg = pl.n_tg;
+    P.n_wblk = pl.n_wblk;
+    P.n_kb = pl.n_kb;
+    P.n_split = pl.n_split;
+    P.stages = pl.stages;
+    P.wait_ns = wait_limit_ns();
+    P.idesc = (1u << 4)                                   // D = f32
+              | ((p.dtype == CT_BF16 ? 1u : 0u) << 7)     // A = bf16 / f16
+              | ((p.dtype == CT_BF16 ? 1u : 0u) << 10)    // B = bf16 / f16
+              | (1u << 16)                                // B MN-major
+              | ((uint32_t)(128 >> 3) << 17)              // N = 128 output channels
+              | ((uint32_t)(128 >> 4) << 24);             // M = 128 input channels
+    auto enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const CUtensorMapDataType dt =
+        p.dtype == CT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    {
+        const cuuint64_t dims[5] = {(cuuint64_t)p.I[2], (cuuint64_t)p.I[1], (cuuint64_t)p.I[0],
+                                    (cuuint64_t)p.C_in, (cuuint64_t)p.B};
+        const cuuint64_t row = (cuuint64_t)p.I[2] * 2;
+        const cuuint64_t strides[4] = {row, row * p.I[1], row * p.I[1] * p.I[0],
+                                       row * p.I[1] * p.I[0] * p.C_in};
+        const cuuint32_t box[5] = {64, 1, 1, 128, 1};
+        const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+        CUresult r = enc(&P.tmap_x, dt, 5, const_cast<void*>(x), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[5] = {(cuuint64_t)pl.C_pad, (cuuint64_t)p.O[2], (cuuint64_t)p.O[1],
+                                    (cuuint64_t)p.O[0], (cuuint64_t)p.B};
+        const cuuint64_t row = (cuuint64_t)pl.C_pad * 2;
+        const cuuint64_t strides[4] = {row, row * p.O[2], row * p.O[2] * p.O[1],
+                                       row * p.O[2] * p.O[1] * p.O[0]};
+        const cuuint32_t box[5] = {64, (cuuint32_t)(64 * p.S[2]), 1, 1, 1};
+        const cuuint32_t es[5] = {1, (cuuint32_t)p.S[2], 1, 1, 1};
+        CUresult r = enc(&P.tmap_dy, dt, 5, dyc, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    cudaError_t e;
+    {
+        // dy -> dy' (channels-last), the same layout kernel as the forward's x
+        TcPrep Q;
+        std::memset(&Q, 0, sizeof(Q));
+        Q.x = dy;
+        Q.xc = dyc;
+        Q.C = (int)p.C_out;
+        Q.C_pad = pl.C_pad;
+        Q.B = (int)p.B;
+        Q.S = p.out_spatial();
+        Q.n_st = (int)((Q.S + 63) / 64);
+        Q.n_ct = pl.C_pad / 64;
+        Q.n_wb = 0;
+        Q.vec = (Q.S % 8) == 0 && ((uintptr_t)dy % 16) == 0;
+        const int64_t blocks = (int64_t)Q.n_st * Q.n_ct * p.B;
+        if ((Q.S + 63) / 64 >= (1ll << 31) || blocks >= (1ll << 31)) return cudaErrorInvalidConfiguration;
+        tc_prepare<T><<<(unsigned)blocks, 256, 0, stream>>>(Q);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    {
+        const size_t smem = (size_t)pl.stages * 128 * 128 * (1 + kDwNT) + 1024;
+        e = cudaFuncSetAttribute(tc_dw_gemm<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(pl.n_icb * pl.n_ocb * pl.n_tg * pl.n_split));
+        cfg.blockDim = dim3(kDwThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, tc_dw_gemm<T>, P);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t n = p.taps() * p.C_in * p.C_out;
+    const int rb = (int)std::min<int64_t>((n + 255) / 256, 152 * 8);
+    tc_dw_reduce<T><<<rb, 256, 0, stream>>>(part, static_cast<T*>(dw), (int)p.C_in, (int)p.C_out,
+                                            (int)p.taps(), pl.n_split);
+    return cudaGetLastError();
+}
+
+int sm_count_or_default() {
+    DeviceInfo d;
+    return device_info(&d) == cudaSuccess ? d.sm_count : 152;
+}
+
 }  // namespace
+
+bool tc_dw_supports(const Problem& p) {
+    DwPlan pl;
+    if (!make_plan_dw(p, sm_count_or_default(), &pl)) return false;
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess) return false;
+    return d.cc_major == 10 && d.cc_minor == 3;
+}
+
+size_t tc_dw_workspace_bytes(const Problem& p) {
+    DwPlan pl;
+    if (!make_plan_dw(p, sm_count_or_default(), &pl)) return 0;
+    return round256(pl.x_bytes) + round256(pl.part_bytes);
+}
+
+cudaError_t launch_tc_dw(const Problem& p, const void* x, const void* dy, void* dw, void* workspace,
+                         cudaStream_t stream) {
+    DwPlan pl;
+    if (!make_plan_dw(p, sm_count_or_default(), &pl) || pl.n_kb == 0) return cudaErrorInvalidValue;
+    if ((uintptr_t)x % 16 != 0) return cudaErrorInvalidValue;
+    if (p.dtype == CT_BF16) return launch_tc_dw_t<__nv_bfloat16>(p, pl, x, dy, dw, workspace, stream);
+    return launch_tc_dw_t<__half>(p, pl, x, dy, dw, workspace, stream);
+}
 
 bool tc_dx_supports(const Problem& p) {
     TcPlan pl;
