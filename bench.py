@@ -527,7 +527,7 @@ def backward_per_config(dev, flush, peaks):
     HBM bandwidth (dy read once)."""
     import transposed_convolution_convtranspose1_gb300 as ct
     out = {"format": "[ms, fraction of peak]: dx, dw of the fp32 FMA peak (of the bf16 tensor peak "
-                     "when marked t: tcgen05 kernel), db of HBM"}
+                     "when marked t: tcgen05 kernel; of the 3xTF32 peak when marked t32), db of HBM"}
     for p in synth.WORKLOADS:
         x, w, _ = synth.make_inputs(p)
         x, w = x.to(dev), w.to(dev)
@@ -567,6 +567,10 @@ def backward_per_config(dev, flush, peaks):
                 nbytes = dy.numel() * dy.element_size() + p.C_out * dy.element_size()
                 ach = nbytes / (ms * 1e-3) / 1e9
                 res[name] = [round(ms, 5), round(ach / peaks["hbm_gbs"], 4)]
+            elif kern[name] == "tc32_phase_gemm":
+                # fp32 on TF32 tensor cores, three products each: the 3xTF32 peak
+                ach = flops / (ms * 1e-3) / 1e12
+                res[name] = [round(ms, 5), round(ach / (peaks["bf16_tflops"] * TF32_PER_BF16 / 3), 4), "t32"]
             elif kern[name] in ("tc_phase_gemm", "tc_dw_gemm"):
                 ach = flops / (ms * 1e-3) / 1e12
                 res[name] = [round(ms, 5), round(ach / peaks["bf16_tflops"], 4), "t"]

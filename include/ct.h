@@ -357,10 +357,11 @@ int ct_conv_transpose_backward_nd(const void* x, const void* w, const void* dy,
                                   int dtype, void* stream);
 
 /*
- * Workspace bytes of ct_conv_transpose_backward_nd: the larger of dw's
- * per-slice partials and, when dx runs on the tensor cores (bf16/fp16,
- * groups of 1, at least 16 channels each side), dy's channels-last copy and
- * the gathered weights.  Covers a call that requests any of dx, dw and db.
+ * Workspace bytes of ct_conv_transpose_backward_nd: the largest of dw's
+ * per-slice partials (or, on the tensor cores, dy's channels-last copy and
+ * the split partials) and, when dx runs on the tensor cores, dy's
+ * channels-last copy (fp32: as TF32 high and low parts) and the gathered
+ * weights.  Covers a call that requests any of dx, dw and db.
  */
 int ct_conv_transpose_backward_workspace_bytes(int nd, int64_t B, int64_t C_in,
                                                int64_t C_out,
@@ -376,7 +377,9 @@ int ct_conv_transpose_backward_workspace_bytes(int nd, int64_t B, int64_t C_in,
  * gradient and of the weight gradient of ct_conv_transpose_backward_nd on
  * this problem, written to *dx_kernel and *dw_kernel as pointers to static
  * strings: "tc_phase_gemm" (dx on the tensor cores: bf16/fp16, groups of 1,
- * at least 16 channels each side) or "bwd_dx_kernel"; "tc_dw_gemm" (dw on
+ * at least 16 channels each side), "tc32_phase_gemm" (dx on the
+ * error-compensated TF32 tensor-core GEMM: fp32, groups of 1, at least 32
+ * channels each side) or "bwd_dx_kernel"; "tc_dw_gemm" (dw on
  * the tensor cores: the same class with a W stride of at most 4 and an input
  * width that is a multiple of 8), "bwd_dw_grouped_kernel" (groups of at most
  * 8 input and 8 output channels, at most 27 taps) or "bwd_dw_kernel"; "" for

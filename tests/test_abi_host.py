@@ -255,5 +255,6 @@ def test_backward_kernel_query_validates_on_the_host(lib):
     assert rc == ctb.CT_ERR_NULL
     dx, dw = q(2, 64, 32, (9, 9), (3, 3), (2, 2), dtype=ctb.CT_BF16)
     assert dx in ("tc_phase_gemm", "bwd_dx_kernel") and dw in ("tc_dw_gemm", "bwd_dw_kernel")
+    assert q(2, 64, 32, (9, 9), (3, 3), (2, 2))[0] in ("tc32_phase_gemm", "bwd_dx_kernel")
     assert q(2, 16, 16, (9, 9), (3, 3), (2, 2), groups=2)[1] == "bwd_dw_grouped_kernel"
     assert q(0, 16, 16, (9, 9), (3, 3), (2, 2))[0] == ""

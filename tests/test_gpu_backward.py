@@ -162,12 +162,14 @@ def test_backward_kernel_query_names_the_kernels_that_run():
             p.output_padding, p.groups, ct.dtype_code(p.torch_dtype))
     assert names(synth.workload(2)) == ("tc_phase_gemm", "tc_dw_gemm")
     assert names(synth.workload(4)) == ("tc_phase_gemm", "tc_dw_gemm")
-    assert names(synth.workload(1)) == ("bwd_dx_kernel", "bwd_dw_kernel")
+    assert names(synth.workload(1)) == ("tc32_phase_gemm", "bwd_dw_kernel")
     assert names(synth.workload(3)) == ("bwd_dx_kernel", "bwd_dw_grouped_kernel")
     for p in TC_DX:
         assert names(p)[0] == "tc_phase_gemm", p.name
     for p in TC_DW:
         assert names(p)[1] == "tc_dw_gemm", p.name
+    for p in TC32_DX:
+        assert names(p)[0] == "tc32_phase_gemm", p.name
     for p in SMALL_GROUPS:
         if p.name != "sg_36taps":
             assert names(p)[1] == "bwd_dw_grouped_kernel", p.name
@@ -198,6 +200,26 @@ def test_backward_tensor_core_dw_matches_oracle(p):
     _, rdw, _ = oracle.conv_transpose_backward(x, w, dy, **p.attrs(), need=("dw",))
     _, dw, _ = _gpu_grads(p, x, w, dy, need=("dw",))
     _check(p, dw, rdw, "dw")
+
+
+# fp32 dx on the error-compensated TF32 GEMM (one group, >= 32 channels): the
+# same mapping; a 1-D row of 300 positions at stride 4 takes four boxes per
+# tile row, and a 2-D and a 3-D case with dilation and output_padding.
+TC32_DX = [
+    P("tc32dx_1d_s4", 2, 64, 48, (300,), 8, stride=4, pad=2, seed=3301),
+    P("tc32dx_2d", 2, 40, 72, (9, 12), 3, stride=2, pad=1, output_padding=1, seed=3302),
+    P("tc32dx_3d_dil", 1, 32, 33, (3, 5, 8), 3, stride=(1, 2, 2), pad=1, dilation=(1, 2, 1),
+      output_padding=(0, 1, 1), seed=3303),
+]
+
+
+@pytest.mark.parametrize("p", TC32_DX, ids=lambda p: p.name)
+def test_backward_tf32_dx_matches_oracle(p):
+    x, w, _ = synth.make_inputs(p)
+    dy = _dy_for(p, 79)
+    rdx, _, _ = oracle.conv_transpose_backward(x, w, dy, **p.attrs(), need=("dx",))
+    dx, _, _ = _gpu_grads(p, x, w, dy, need=("dx",))
+    _check(p, dx, rdx, "dx")
 
 
 @pytest.mark.parametrize("p", TC_DX, ids=lambda p: p.name)

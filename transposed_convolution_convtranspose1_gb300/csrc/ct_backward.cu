@@ -1058,6 +1058,11 @@ cudaError_t launch_backward_t(const Problem& p, const BwdPlan& pl, BwdArgs a, cu
         e = launch_tc_dx(p, a.dy, a.w, a.dx, a.part, stream);
         *launches += 2;
         if (e != cudaSuccess) return e;
+    } else if (a.dx && p.x_elems() > 0 && tc32_dx_supports(p)) {
+        // fp32: the same mapping on the error-compensated TF32 GEMM
+        e = launch_tc32_dx(p, a.dy, a.w, a.dx, a.part, stream);
+        *launches += 2;
+        if (e != cudaSuccess) return e;
     } else if (a.dx) {
         switch (pl.icb) {
             case 1: e = launch_dx_t<T, 1>(a, pl, stream); break;
@@ -1117,7 +1122,8 @@ cudaError_t backward_error_word(unsigned int* v, bool clear) {
 
 const char* backward_dx_kernel_name(const Problem& p) {
     if (p.x_elems() == 0) return "";
-    return tc_dx_supports(p) ? "tc_phase_gemm" : "bwd_dx_kernel";
+    if (tc_dx_supports(p)) return "tc_phase_gemm";
+    return tc32_dx_supports(p) ? "tc32_phase_gemm" : "bwd_dx_kernel";
 }
 
 const char* backward_dw_kernel_name(const Problem& p) {
@@ -1145,6 +1151,7 @@ size_t backward_workspace_bytes(const Problem& p, bool dx, bool dw) {
     size_t need = dw ? (pl.part_bytes + 255) / 256 * 256 : 0;
     if (dw && p.w_elems() > 0 && tc_dw_supports(p)) need = std::max(need, tc_dw_workspace_bytes(p));
     if (dx && p.x_elems() > 0 && tc_dx_supports(p)) need = std::max(need, tc_dx_workspace_bytes(p));
+    if (dx && p.x_elems() > 0 && tc32_dx_supports(p)) need = std::max(need, tc32_dx_workspace_bytes(p));
     return need;
 }
 

@@ -73,6 +73,11 @@ bool tc_dx_supports(const Problem& p);
 size_t tc_dx_workspace_bytes(const Problem& p);
 cudaError_t launch_tc_dx(const Problem& p, const void* dy, const void* w, void* dx, void* workspace,
                          cudaStream_t stream);
+// The input gradient on the error-compensated TF32 GEMM (fp32, groups of 1): ct_tc32.cu.
+bool tc32_dx_supports(const Problem& p);
+size_t tc32_dx_workspace_bytes(const Problem& p);
+cudaError_t launch_tc32_dx(const Problem& p, const void* dy, const void* w, void* dx, void* workspace,
+                           cudaStream_t stream);
 // The weight gradient on the tcgen05 GEMM (16-bit types, groups of 1): ct_tc.cu.
 bool tc_dw_supports(const Problem& p);
 size_t tc_dw_workspace_bytes(const Problem& p);

@@ -98,6 +98,10 @@ struct Tc32Params {
     int ntap[3][kMaxS];
     int tap[3][kMaxS][kMaxTaps];
     int off[3][kMaxS][kMaxTaps];
+    int cmul[3];            // X'' coordinate of tile position q on each axis: q * cmul + tap offset
+    int nwbox;              // X'' boxes per k-block and plane along W (one row of WC positions, MR = 1)
+    int wbox_step;          // W coordinate step between them
+    uint32_t wbox_bytes;    // shared-memory bytes of one
     int n_classes, total_tiles;
     int n_full, total_slots;  // tiles run whole; work slots (the rest run as two halves)
     int g_qd, g_qh, g_qw;   // spatial tile grid (largest over the phases)
@@ -240,9 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
                         const int tap =
                             (P.tap[0][C.rd][jd] * P.Kdims[1] + P.tap[1][C.rh][jh]) * P.Kdims[2] +
                             P.tap[2][C.rw][jw];
-                        const int id = tl.qd + P.off[0][C.rd][jd];
-                        const int ih = tl.qh0 + P.off[1][C.rh][jh];
-                        const int iw = tl.qw0 + P.off[2][C.rw][jw];
+                        const int id = tl.qd * P.cmul[0] + P.off[0][C.rd][jd];
+                        const int ih = tl.qh0 * P.cmul[1] + P.off[1][C.rh][jh];
+                        const int iw = tl.qw0 * P.cmul[2] + P.off[2][C.rw][jw];
                         for (int kb = 0; kb < P.n_kblk; ++kb) {
                             ok = issued < (uint32_t)P.stages ||  // a fresh slot is free
                                  __all_sync(0xffffffffu,
@@ -256,10 +260,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_phase_gemm(const __grid_cons
                                 tma_load_3d(sa, &P.tmap_w, fb, kb * kBlockK, tl.oc0, tap);
                                 tma_load_3d(sa + kPlaneA, &P.tmap_w, fb, kb * kBlockK, tl.oc0,
                                             P.taps + tap);
-                                tma_load_5d(sa + 2 * kPlaneA, &P.tmap_x, fb, kb * kBlockK, iw, ih,
-                                            id, tl.b);
-                                tma_load_5d(sa + 2 * kPlaneA + planeB, &P.tmap_x, fb, kb * kBlockK,
-                                            iw, ih, id, P.B + tl.b);
+                                for (int xb = 0; xb < P.nwbox; ++xb) {
+                                    const uint32_t o = 2 * kPlaneA + xb * P.wbox_bytes;
+                                    tma_load_5d(sa + o, &P.tmap_x, fb, kb * kBlockK, iw + xb * P.wbox_step,
+                                                ih, id, tl.b);
+                                    tma_load_5d(sa + o + planeB, &P.tmap_x, fb, kb * kBlockK,
+                                                iw + xb * P.wbox_step, ih, id, P.B + tl.b);
+                                }
                             }
                             __syncwarp();
                             ++issued;
@@ -549,15 +556,29 @@ struct Tc32Prep {
     int C, C_pad, B, C_out, taps, N_pad;
     int64_t S;
     int n_st, n_ct, n_jt;  // x tiles along s and c; weight tiles along j
-    int64_t n_wb;          // weight tiles (first blocks of the grid)
+    int64_t n_wb;          // weight blocks (first blocks of the grid)
     bool vec;
+    bool w_gather;         // W''[p][tap][n][c] from w[n][c][tap] (input gradient), 256 elements per block
 };
 
 __global__ void __launch_bounds__(256) tc32_prepare(const __grid_constant__ Tc32Prep Q) {
     // the GEMM that follows may begin its prologue now
     asm volatile("griddepcontrol.launch_dependents;");
     const int64_t bid = blockIdx.x;
-    if (bid < Q.n_wb) {
+    if (bid < Q.n_wb && Q.w_gather) {
+        // input gradient: W''[tap][n][c] = w[n][c][tap] (n < C_out, c < C, else 0), hi and lo planes
+        const int64_t e = bid * 256 + threadIdx.x;
+        const int64_t plane = (int64_t)Q.taps * Q.N_pad * Q.C_pad;
+        if (e < plane) {
+            const int tp = (int)(e / ((int64_t)Q.N_pad * Q.C_pad));
+            const int n = (int)((e / Q.C_pad) % Q.N_pad), c = (int)(e % Q.C_pad);
+            const float v = n < Q.C_out && c < Q.C ? __ldg(Q.w + ((int64_t)n * Q.C + c) * Q.taps + tp) : 0.f;
+            float hi, lo;
+            split_tf32(v, hi, lo);
+            Q.wp[e] = hi;
+            Q.wp[plane + e] = lo;
+        }
+    } else if (bid < Q.n_wb) {
         const int64_t wb = bid;
         const int jt = (int)(wb % Q.n_jt), ct = (int)(wb / Q.n_jt);
         tc32_weight_tile(Q.w, Q.wp, Q.C, Q.C_out, Q.taps, Q.N_pad, Q.C_pad, ct * 32, (int64_t)jt * 64);
@@ -576,6 +597,7 @@ __global__ void __launch_bounds__(256) tc32_prepare(const __grid_constant__ Tc32
 
 struct Tc32Plan {
     int C_pad, N_pad, n_oc_tiles, WC, MR, stages;
+    int nwbox = 1;          // X'' boxes per row of a tile (input gradient, strided W)
     size_t x_bytes, w_bytes, stage_bytes, epi_bytes;
     AxisPlan ax[3];
 };
@@ -614,9 +636,18 @@ bool make_plan(const Problem& p, Tc32Plan* pl) {
     return true;
 }
 
+// How the GEMM reads its operands when it computes an input gradient (see
+// make_plan_dx): X'' coordinates q * cmul + offset, X'' boxes that take every
+// es-th position on W and H (TMA element strides), W'' gathered as w[n][c][tap].
+struct Tc32Operands {
+    int cmul[3];
+    int es_w, es_h;
+    bool w_gather;
+};
+
 cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x, const void* w,
                              const void* bias, void* y, void* workspace, cudaStream_t stream,
-                             Profile* prof) {
+                             Profile* prof, const Tc32Operands* ops = nullptr) {
     DeviceInfo dev;
     cudaError_t e = device_info(&dev);
     if (e != cudaSuccess) return e;
@@ -633,6 +664,10 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
     P.n_kblk = pl.C_pad / kBlockK;
     P.n_oc_tiles = pl.n_oc_tiles;
     P.taps = (int)p.taps();
+    for (int a = 0; a < 3; ++a) P.cmul[a] = ops ? ops->cmul[a] : 1;
+    P.nwbox = pl.nwbox;
+    P.wbox_step = (pl.WC / pl.nwbox) * (ops ? ops->es_w : 1);
+    P.wbox_bytes = (uint32_t)(pl.WC / pl.nwbox) * kBlockK * 4;
     for (int a = 0; a < 3; ++a) {
         P.O[a] = (int)p.O[a];
         P.S[a] = p.S[a];
@@ -733,8 +768,11 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
         const cuuint64_t row = (cuuint64_t)pl.C_pad * 4;
         const cuuint64_t strides[4] = {row, row * p.I[2], row * p.I[2] * p.I[1],
                                        row * p.I[2] * p.I[1] * p.I[0]};
-        const cuuint32_t box[5] = {(cuuint32_t)kBlockK, (cuuint32_t)pl.WC, (cuuint32_t)pl.MR, 1, 1};
-        const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+        // with element strides the box spans es x the positions it loads
+        const cuuint32_t esw = ops ? (cuuint32_t)ops->es_w : 1u, esh = ops ? (cuuint32_t)ops->es_h : 1u;
+        const cuuint32_t box[5] = {(cuuint32_t)kBlockK, (cuuint32_t)(pl.WC / pl.nwbox) * esw,
+                                   (cuuint32_t)pl.MR * esh, 1, 1};
+        const cuuint32_t es[5] = {1, esw, esh, 1, 1};
         CUresult r = enc(&P.tmap_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, xc, dims, strides, box, es,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -752,6 +790,8 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
         Q.n_ct = pl.C_pad / 32;
         Q.n_jt = (int)(((int64_t)pl.N_pad * p.taps() + 63) / 64);
         Q.n_wb = (int64_t)Q.n_jt * Q.n_ct;
+        Q.w_gather = ops && ops->w_gather;
+        if (Q.w_gather) Q.n_wb = ((int64_t)p.taps() * pl.N_pad * pl.C_pad + 255) / 256;
         Q.vec = (Q.S % 4) == 0 && ((uintptr_t)x % 16) == 0;
         const int64_t blocks = Q.n_wb + (int64_t)Q.n_st * Q.n_ct * p.B;
         if ((Q.S + 63) / 64 >= (1ll << 31) || blocks >= (1ll << 31)) return cudaErrorInvalidConfiguration;
@@ -788,7 +828,94 @@ cudaError_t launch_tc32_impl(const Problem& p, const Tc32Plan& pl, const void* x
     return e;
 }
 
+// The input gradient as a GEMM on this kernel (fp32, groups of 1; see the
+// bf16/fp16 route's make_plan_dx for the mapping): one output phase of
+// stride 1, dy's channels as the reduction, all taps at X'' offsets
+// t * d - pad_lo, tile position q read at X'' coordinate q * s through TMA
+// element strides on W and H.
+bool make_plan_dx(const Problem& p, Tc32Plan* pl, Problem* pd, Tc32Operands* ops) {
+    if (p.dtype != CT_F32 || p.G != 1) return false;
+    for (int a = 0; a < 3; ++a)
+        if (p.K[a] > kMaxTaps || p.S[a] > kMaxS) return false;
+    *pd = p;
+    pd->C_in = p.C_out;
+    pd->C_out = p.C_in;
+    pd->Cig = (int)pd->C_in;
+    pd->Cog = (int)pd->C_out;
+    pd->act = 0;
+    for (int a = 0; a < 3; ++a) {
+        pd->I[a] = p.O[a];
+        pd->O[a] = p.I[a];
+        pd->S[a] = 1;
+        AxisPlan& ax = pl->ax[a];
+        std::memset(&ax, 0, sizeof(ax));
+        ax.s = 1;
+        ax.q_extent[0] = p.I[a];
+        ax.ntaps[0] = (int)p.K[a];
+        for (int j = 0; j < p.K[a]; ++j) {
+            ax.tap[0][j] = j;
+            ax.off[0][j] = j * p.DL[a] - p.PL[a];
+        }
+        ops->cmul[a] = p.S[a];
+    }
+    ops->es_w = p.S[2];
+    ops->es_h = p.S[1];
+    ops->w_gather = true;
+    pl->N_pad = (int)((pd->C_out + kBlockM - 1) / kBlockM * kBlockM);
+    pl->n_oc_tiles = pl->N_pad / kBlockM;
+    pl->C_pad = (int)((pd->C_in + kCAlign - 1) / kCAlign * kCAlign);
+    // a box spans at most 256 traversed positions (256 / s_W loaded); a tile
+    // row of more positions takes several boxes, when it is the tile's only row
+    int wbox = 32;  // an epilogue block (32 positions) stays within one row
+    while (wbox < p.I[2] && wbox < kNP && wbox * 2 * p.S[2] <= 256) wbox *= 2;
+    int wc = wbox;
+    while (wc < p.I[2] && wc < kNP) wc *= 2;
+    if (wc > wbox && wc != kNP) wc = wbox;  // several boxes only for a one-row tile
+    pl->WC = wc;
+    pl->MR = kNP / wc;
+    pl->nwbox = wc / wbox;
+    if (wbox * p.S[2] > 256 || pl->MR * p.S[1] > 256) return false;  // TMA box extents
+    pl->stage_bytes = 2 * (size_t)kPlaneA + 2 * (size_t)kNP * kBlockK * 4;
+    pl->epi_bytes = (size_t)kEpiWarps * 32 * 32 * 4;
+    const size_t room = kSmemLimit - 1024 - 1024 - pl->epi_bytes;
+    pl->stages = (int)std::min<size_t>(8, room / pl->stage_bytes);
+    if (pl->stages < 2) return false;
+    pl->x_bytes = 2 * (size_t)p.B * p.out_spatial() * pl->C_pad * 4;
+    pl->w_bytes = 2 * (size_t)p.taps() * pl->N_pad * pl->C_pad * 4;
+    if ((double)p.out_spatial() * pl->C_pad * 4 * p.B >= 1e12) return false;
+    if (2 * p.B >= (1ll << 31) || 2 * p.taps() >= (1ll << 31)) return false;
+    return true;
+}
+
 }  // namespace
+
+bool tc32_dx_supports(const Problem& p) {
+    Tc32Plan pl;
+    Problem pd;
+    Tc32Operands ops;
+    if (!make_plan_dx(p, &pl, &pd, &ops)) return false;
+    if (p.C_in < 32 || p.C_out < 32) return false;  // small channel counts: the CUDA-core kernel
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess) return false;
+    return d.cc_major == 10 && d.cc_minor == 3;
+}
+
+size_t tc32_dx_workspace_bytes(const Problem& p) {
+    Tc32Plan pl;
+    Problem pd;
+    Tc32Operands ops;
+    if (!make_plan_dx(p, &pl, &pd, &ops)) return 0;
+    return round256(pl.x_bytes) + round256(pl.w_bytes);
+}
+
+cudaError_t launch_tc32_dx(const Problem& p, const void* dy, const void* w, void* dx, void* workspace,
+                           cudaStream_t stream) {
+    Tc32Plan pl;
+    Problem pd;
+    Tc32Operands ops;
+    if (!make_plan_dx(p, &pl, &pd, &ops)) return cudaErrorInvalidValue;
+    return launch_tc32_impl(pd, pl, dy, w, nullptr, dx, workspace, stream, nullptr, &ops);
+}
 
 bool tc32_supports(const Problem& p) {
     Tc32Plan pl;
