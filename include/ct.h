@@ -357,7 +357,8 @@ int ct_conv_transpose_backward_nd(const void* x, const void* w, const void* dy,
                                   int dtype, void* stream);
 
 /*
- * Workspace bytes of ct_conv_transpose_backward_nd: the largest of dw's
+ * Workspace bytes of ct_conv_transpose_backward_nd: the largest of db's
+ * per-segment partials (a few floats per output channel), dw's
  * per-slice partials (or, on the tensor cores, dy's channels-last copy and
  * the split partials) and, when dx runs on the tensor cores, dy's
  * channels-last copy (fp32: as TF32 high and low parts) and the gathered

@@ -695,7 +695,7 @@ int ct_conv_transpose_backward_nd(const void* x, const void* w, const void* dy, 
         return fail(CT_ERR_TOO_LARGE, "backward: %lld taps per input channel block exceed the staged slab",
                     (long long)p.taps());
     cudaStream_t s = (cudaStream_t)stream;
-    const size_t need = backward_workspace_bytes(p, dx != nullptr, dw != nullptr);
+    const size_t need = backward_workspace_bytes(p, dx != nullptr, dw != nullptr, db != nullptr);
     void* ws = workspace;
     bool owned = false;
     if (need > 0) {

@@ -15,9 +15,10 @@
 // db a per-channel sum.  Kernels (fp32 accumulation, one rounding to the
 // tensor dtype, no atomics: every result is summed in a fixed order, so runs
 // are bit-reproducible):
-//   bwd_db_kernel   one block per output channel; each thread sums a strided
-//                   share of the channel in four compensated (Kahan) fp32
-//                   sums, then a fixed shared-memory tree.
+//   bwd_db_partial  a block per (output channel, run of its On positions, all
+//                   batch elements); each thread sums 8-value vectors in four
+//                   compensated (Kahan) fp32 sums, then a fixed shared-memory
+//                   tree; bwd_db_final adds a channel's segments in order.
 //   bwd_dx_kernel   one thread per input position and ICB input channels of
 //                   a group; the group's weights for a chunk of output
 //                   channels are staged in shared memory ([oc][tap][ICB]) and
@@ -78,33 +79,59 @@ struct BwdArgs {
 // db
 // ---------------------------------------------------------------------------
 
-constexpr int kDbThreads = 512;
+constexpr int kDbThreads = 256;
 
+// db in two passes.  Pass 1: block (oc, k) sums channel oc over every batch
+// element and the k-th run [k seg, (k+1) seg) of its On positions (seg a
+// multiple of 8), each thread in four compensated (Kahan) sums over 8-value
+// vectors, a vector of every batch element before the next vector (one 16-byte load for 16-bit types, two for fp32, when On is a
+// multiple of 8 and dy is 16-byte aligned), then a fixed shared-memory tree;
+// the block writes part[oc][k].  Pass 2 adds each channel's partials in order
+// (compensated) and rounds once.
 template <typename T>
-__global__ void __launch_bounds__(kDbThreads) bwd_db_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(kDbThreads) bwd_db_partial(const __grid_constant__ BwdArgs a, float* part,
+                                                             int n_seg, int64_t seg, bool vec) {
     __shared__ float red[kDbThreads];
-    const int64_t oc = blockIdx.x;
+    const int64_t oc = blockIdx.x / n_seg;
+    const int k = (int)(blockIdx.x % n_seg);
     const T* __restrict__ dy = static_cast<const T*>(a.dy);
-    // four independent compensated (Kahan) sums per thread, so that four
-    // loads are in flight; comp holds each sum's lost low-order part
+    const int64_t o0 = (int64_t)k * seg, o1 = min(a.On, o0 + seg);
     float sum[4] = {0.f, 0.f, 0.f, 0.f}, comp[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int64_t b = 0; b < a.B; ++b) {
-        const T* p = dy + (b * a.C_out + oc) * a.On;
-        for (int64_t o = threadIdx.x; o < a.On; o += 4 * kDbThreads) {
-            float v[4];
+    auto add = [&](int u, float v) {
+        const float y = v - comp[u];
+        const float t = sum[u] + y;
+        comp[u] = (t - sum[u]) - y;
+        sum[u] = t;
+    };
+    // a thread's position vector of every batch element in turn: B independent
+    // loads per vector, so several are in flight
+    const T* chan = dy + oc * a.On;
+    const int64_t bstride = a.C_out * a.On;
+    if (vec) {
+        for (int64_t o = o0 + 8 * (int64_t)threadIdx.x; o < o1; o += 8 * kDbThreads) {
+#pragma unroll 4
+            for (int64_t b = 0; b < a.B; ++b) {
+                const T* q = chan + b * bstride + o;
+                float v[8];
+                if constexpr (sizeof(T) == 2) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(q);
+                    const T* h = reinterpret_cast<const T*>(&u);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int64_t ou = o + (int64_t)u * kDbThreads;
-                v[u] = ou < a.On ? to_f32(p[ou]) : 0.f;
-            }
+                    for (int j = 0; j < 8; ++j) v[j] = to_f32(h[j]);
+                } else {
+                    const float4 q0 = reinterpret_cast<const float4*>(q)[0];
+                    const float4 q1 = reinterpret_cast<const float4*>(q)[1];
+                    v[0] = q0.x; v[1] = q0.y; v[2] = q0.z; v[3] = q0.w;
+                    v[4] = q1.x; v[5] = q1.y; v[6] = q1.z; v[7] = q1.w;
+                }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float y = v[u] - comp[u];
-                const float t = sum[u] + y;
-                comp[u] = (t - sum[u]) - y;
-                sum[u] = t;
+                for (int j = 0; j < 8; ++j) add(j & 3, v[j]);
             }
         }
+    } else {
+        for (int64_t o = o0 + threadIdx.x; o < o1; o += kDbThreads)
+#pragma unroll 4
+            for (int64_t b = 0; b < a.B; ++b) add((int)(b & 3), to_f32(chan[b * bstride + o]));
     }
     red[threadIdx.x] = (sum[0] + sum[1]) + (sum[2] + sum[3]);
     __syncthreads();
@@ -112,7 +139,34 @@ __global__ void __launch_bounds__(kDbThreads) bwd_db_kernel(const __grid_constan
         if ((int)threadIdx.x < h) red[threadIdx.x] += red[threadIdx.x + h];
         __syncthreads();
     }
-    if (threadIdx.x == 0) static_cast<T*>(a.db)[oc] = from_f32<T>(red[0]);
+    if (threadIdx.x == 0) part[oc * n_seg + k] = red[0];
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_db_final(const float* __restrict__ part, T* __restrict__ db, int64_t C_out,
+                                                    int n_seg) {
+    const int64_t oc = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (oc >= C_out) return;
+    float sum = 0.f, comp = 0.f;
+    for (int k = 0; k < n_seg; ++k) {
+        const float y = part[oc * n_seg + k] - comp;
+        const float t = sum + y;
+        comp = (t - sum) - y;
+        sum = t;
+    }
+    db[oc] = from_f32<T>(sum);
+}
+
+// Position runs of each channel for bwd_db_partial: about eight resident
+// 256-thread blocks per SM in all, each run at least 2048 positions.
+void db_split(const Problem& p, int sm_count, int* n_seg, int64_t* seg) {
+    const int64_t n = p.out_spatial();
+    const int64_t want = std::max<int64_t>(1, 8ll * std::max(1, sm_count) / std::max<int64_t>(1, p.C_out));
+    const int64_t k = std::max<int64_t>(1, std::min<int64_t>(want, (n + 2047) / 2048));
+    int64_t s = (n + k - 1) / k;
+    s = (s + 7) / 8 * 8;
+    *seg = std::max<int64_t>(8, s);
+    *n_seg = (int)std::max<int64_t>(1, (n + *seg - 1) / *seg);
 }
 
 // ---------------------------------------------------------------------------
@@ -1047,7 +1101,19 @@ cudaError_t launch_backward_t(const Problem& p, const BwdPlan& pl, BwdArgs a, cu
                               int* launches) {
     cudaError_t e = cudaSuccess;
     if (a.db && p.C_out > 0) {
-        bwd_db_kernel<T><<<(unsigned)p.C_out, kDbThreads, 0, stream>>>(a);
+        // the partials use the workspace before dx and dw do (same stream)
+        int n_seg;
+        int64_t seg;
+        db_split(p, pl.sm_count, &n_seg, &seg);
+        float* part = a.part;
+        const bool vec = p.out_spatial() % 8 == 0 && (uintptr_t)a.dy % 16 == 0;
+        const int64_t blocks = p.C_out * n_seg;
+        if (blocks >= (1ll << 31)) return cudaErrorInvalidConfiguration;
+        bwd_db_partial<T><<<(unsigned)blocks, kDbThreads, 0, stream>>>(a, part, n_seg, seg, vec);
+        ++*launches;
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        bwd_db_final<T><<<(unsigned)((p.C_out + 255) / 256), 256, 0, stream>>>(part, static_cast<T*>(a.db), p.C_out,
+                                                                          n_seg);
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
@@ -1142,20 +1208,26 @@ bool backward_supported(const Problem& p) {
     return bwd_plan(p, 152, &pl);
 }
 
-size_t backward_workspace_bytes(const Problem& p, bool dx, bool dw) {
+size_t backward_workspace_bytes(const Problem& p, bool dx, bool dw, bool db) {
     DeviceInfo d;
     int sm = 152;
     if (device_info(&d) == cudaSuccess) sm = d.sm_count;
     BwdPlan pl;
     if (!bwd_plan(p, sm, &pl)) return 0;
     size_t need = dw ? (pl.part_bytes + 255) / 256 * 256 : 0;
+    if (db && p.C_out > 0) {
+        int n_seg;
+        int64_t seg;
+        db_split(p, sm, &n_seg, &seg);
+        need = std::max(need, ((size_t)p.C_out * n_seg * sizeof(float) + 255) / 256 * 256);
+    }
     if (dw && p.w_elems() > 0 && tc_dw_supports(p)) need = std::max(need, tc_dw_workspace_bytes(p));
     if (dx && p.x_elems() > 0 && tc_dx_supports(p)) need = std::max(need, tc_dx_workspace_bytes(p));
     if (dx && p.x_elems() > 0 && tc32_dx_supports(p)) need = std::max(need, tc32_dx_workspace_bytes(p));
     return need;
 }
 
-size_t backward_workspace_bytes(const Problem& p) { return backward_workspace_bytes(p, true, true); }
+size_t backward_workspace_bytes(const Problem& p) { return backward_workspace_bytes(p, true, true, true); }
 
 cudaError_t launch_backward(const Problem& p, const void* x, const void* w, const void* dy, void* dx,
                             void* dw, void* db, void* workspace, cudaStream_t stream, int* launches) {

@@ -60,11 +60,12 @@ cudaError_t launch_tc32(const Problem& p, const void* x, const void* w, const vo
 // dx, dw and db, each skipped when its pointer is null.  The workspace holds
 // dw's per-slice fp32 partials.  `launches` (optional) counts the kernels.
 bool backward_supported(const Problem& p);
-// Workspace of the backward call: the larger of the dw partials and, when dx
+// Workspace of the backward call: the largest of the db partials, the dw
+// partials (or dy's channels-last copy and the split partials) and, when dx
 // runs on the tensor cores, dy's channels-last copy and the gathered weights
-// (stream-ordered, so the two uses share it).
+// (stream-ordered, so the uses share it).
 size_t backward_workspace_bytes(const Problem& p);
-size_t backward_workspace_bytes(const Problem& p, bool dx, bool dw);
+size_t backward_workspace_bytes(const Problem& p, bool dx, bool dw, bool db);
 // Kernels that take most of the device time of dx and of dw.
 const char* backward_dx_kernel_name(const Problem& p);
 const char* backward_dw_kernel_name(const Problem& p);
